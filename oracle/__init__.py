@@ -1,0 +1,154 @@
+"""CPU oracle for the sum reductions.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the CUDA library (``reduction_rdx_sum_gb300``) and imports nothing from
+it; the two meet only in the seeded input generator, which holds none of the
+method's arithmetic.
+
+Contents
+--------
+``oracle.c`` (loaded here through ctypes)
+    The plain definitions, one loop in index order each: float64 Kahan sums for
+    float32 and bfloat16 inputs, int64 sums for int32, per-row loops for the
+    row-segmented sum.  Page "03_shared_memory_sync_reduction.py", demo 3:
+    the expected value of every reduction version is the float64 sum of the
+    input.
+``ladder.py``
+    The five block-level reduction versions of that page's demo 3, restated in
+    numpy float32 in the page's order of operations, giving each block's
+    partial sum bit for bit.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, exact rational sums, brute force on tiny inputs and the page's worked
+example; none is marked "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_CFLAGS = ["-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_liboracle.so`` next to it (gcc, no GPU)."""
+    stale = force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        p, i64, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+        for name in ("oracle_sum_f32", "oracle_sumsq_f32", "oracle_abssum_f32",
+                     "oracle_sum_bf16", "oracle_sumsq_bf16", "oracle_abssum_bf16"):
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = [p, i64], dbl
+        lib.oracle_sum_i32.argtypes, lib.oracle_sum_i32.restype = [p, i64], i64
+        for name in ("oracle_rowsum_f32", "oracle_rowabssum_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = [p, i64, i64, p], None
+        _lib = lib
+        return lib
+
+
+def _flat(x: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"oracle expects {np.dtype(dtype)}, got {a.dtype}")
+    return a.reshape(-1)
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+# ---- float32 -------------------------------------------------------------
+
+def sum_f32(x: np.ndarray) -> float:
+    """Sum of float32 values, float64 Kahan, index order."""
+    a = _flat(x, np.float32)
+    return _load().oracle_sum_f32(_ptr(a), a.size)
+
+
+def sumsq_f32(x: np.ndarray) -> float:
+    """Sum of squares of float32 values (each square exact in float64)."""
+    a = _flat(x, np.float32)
+    return _load().oracle_sumsq_f32(_ptr(a), a.size)
+
+
+def abssum_f32(x: np.ndarray) -> float:
+    """Sum of |x_i|: the scale of the float32 tolerance."""
+    a = _flat(x, np.float32)
+    return _load().oracle_abssum_f32(_ptr(a), a.size)
+
+
+# ---- bfloat16, passed as the raw uint16 bit patterns ----------------------
+
+def sum_bf16(bits: np.ndarray) -> float:
+    """Sum of bfloat16 values (given as uint16 bit patterns), each widened exactly."""
+    a = _flat(bits, np.uint16)
+    return _load().oracle_sum_bf16(_ptr(a), a.size)
+
+
+def sumsq_bf16(bits: np.ndarray) -> float:
+    a = _flat(bits, np.uint16)
+    return _load().oracle_sumsq_bf16(_ptr(a), a.size)
+
+
+def abssum_bf16(bits: np.ndarray) -> float:
+    a = _flat(bits, np.uint16)
+    return _load().oracle_abssum_bf16(_ptr(a), a.size)
+
+
+# ---- int32 -> int64 --------------------------------------------------------
+
+def sum_i32(x: np.ndarray) -> int:
+    """Exact int64 sum of int32 values."""
+    a = _flat(x, np.int32)
+    return int(_load().oracle_sum_i32(_ptr(a), a.size))
+
+
+# ---- row-segmented float32 -------------------------------------------------
+
+def rowsum_f32(x: np.ndarray) -> np.ndarray:
+    """Per-row float64 Kahan sums of a row-major (rows, cols) float32 matrix."""
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.float32 or a.ndim != 2:
+        raise TypeError("rowsum_f32 expects a 2-D float32 array")
+    rows, cols = a.shape
+    out = np.empty(rows, dtype=np.float64)
+    _load().oracle_rowsum_f32(_ptr(a), rows, cols, _ptr(out))
+    return out
+
+
+def rowabssum_f32(x: np.ndarray) -> np.ndarray:
+    """Per-row sums of |x|: the per-row tolerance scale."""
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.float32 or a.ndim != 2:
+        raise TypeError("rowabssum_f32 expects a 2-D float32 array")
+    rows, cols = a.shape
+    out = np.empty(rows, dtype=np.float64)
+    _load().oracle_rowabssum_f32(_ptr(a), rows, cols, _ptr(out))
+    return out
+
+
+from .ladder import LADDER_BLOCK, ladder_partials, ladder_segment, VERSIONS  # noqa: E402,F401

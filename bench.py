@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 sum-reduction library on its workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+A step is one pass of every reduction entry point over its workload's input:
+  fp32 sum and sum of squares of n = 2^24 + 13 normal(0,1) values (seed 1),
+  int32 -> int64 sum of n = 2^28 uniform integers in [-2^20, 2^20] (seed 2),
+  fp32 row sums of 8192 x 32768 and of 2^20 x 256 uniform[-1,1) (seed 3),
+  bf16 -> fp32 sum and sum of squares of n = 2^30 + 7 normal(0,1) (seed 4).
+The metric is GB/s of input read by the reductions (algorithmic bytes / device
+time).  Every launch is timed with CUDA events on the stream it runs on, after
+an untimed 512 MiB write that flushes the L2 (129 MB), so each launch reads its
+input from HBM.  ``e2e`` repeats the step from pinned host memory: the
+host-to-device copies of the inputs and the device-to-host copies of the
+results are inside its timed region.  ``cpu_baseline`` times the CPU oracle
+(one core) on a bounded sample of the same step.
+
+``--impl reference`` times the CPU oracle alone, as the comparison arm, on a
+bounded sample of each step.
+
+Under torchrun each rank reduces its own copy of the workload (weak scaling,
+no collective on the data path); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from reduction_rdx_sum_gb300 import inputs  # noqa: E402
+
+METRIC = "reduction GB/s read (and % of GB300 HBM peak) per config, 1 GPU"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel from one ncu capture, and the hash of the kernel sources it was taken
+# on; reported as null once the sources differ.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "reduction_rdx_sum_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    """Largest value over all ranks (timing is reported for the slowest rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+
+def suite_arrays():
+    """Host inputs of the step; workloads that share a recipe share an array."""
+    arrays, keyed = {}, {}
+    for w in inputs.SUITE:
+        key = (w.dist, w.seed, w.numel)
+        if key not in keyed:
+            keyed[key] = inputs.make(w).reshape(-1)
+        arrays[w.name] = keyed[key]
+    return arrays, keyed
+
+
+def step_bytes():
+    return sum(w.bytes_read for w in inputs.SUITE)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str | None):
+        self.path = path
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w") if self.path else subprocess.PIPE
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20",
+                 "-i", str(self.gpu_index)], stdout=self.out, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                text = self.proc.communicate(timeout=5)[0] if not self.path else None
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                text = None
+            if self.path:
+                self.out.close()
+                with open(self.path) as f:
+                    text = f.read()
+            self.text = text or ""
+        else:
+            self.text = ""
+
+    def summary(self):
+        rows = [r.split(",") for r in self.text.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        power = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (the reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_pass(arrays, frac: float):
+    """Run the oracle over the first `frac` of every workload of the step;
+    returns (bytes processed, seconds)."""
+    import oracle
+
+    total, t0 = 0, time.perf_counter()
+    for w in inputs.SUITE:
+        a = arrays[w.name]
+        if w.op == "rowsum_f32":
+            rows, cols = w.shape
+            r = max(1, int(rows * frac))
+            oracle.rowsum_f32(a[: r * cols].reshape(r, cols))
+            total += r * cols * 4
+            continue
+        k = max(1, int(a.size * frac))
+        getattr(oracle, w.op)(a[:k])
+        total += k * w.itemsize
+    return total, time.perf_counter() - t0
+
+
+def calibrate_oracle(arrays, budget_s: float):
+    """Fraction of the step the oracle finishes in about budget_s seconds."""
+    b, s = oracle_pass(arrays, 1.0 / 256)
+    rate = b / max(s, 1e-9)
+    return min(1.0, budget_s * rate / step_bytes())
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    arrays, _ = suite_arrays()
+    per_step_budget = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    frac = calibrate_oracle(arrays, per_step_budget)
+    for _ in range(args.warmup):
+        oracle_pass(arrays, frac)
+    done, secs = 0, 0.0
+    for _ in range(args.steps):
+        b, s = oracle_pass(arrays, frac)
+        done, secs = done + b, secs + s
+    value = done / secs / 1e9
+    sample = (f"first {frac:.4%} of every workload of the step (about {done / args.steps / 1e6:.0f} MB per step), "
+              "single-threaded C oracle, float64 Kahan / int64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64,i64",
+        "data": "synthetic", "config": config_block(),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block():
+    return {
+        "workload": "rdx suite: fp32 sum+sumsq n=2^24+13 N(0,1) s1; int32->int64 sum n=2^28 U{-2^20..2^20} s2; "
+                    "fp32 rowsum 8192x32768 and 1048576x256 U[-1,1) s3; bf16->fp32 sum+sumsq n=2^30+7 N(0,1) s4",
+        "bytes_read_per_step": step_bytes(),
+        "launches_per_step": len(inputs.SUITE),
+        "l2": f"flushed before every timed launch ({FLUSH_BYTES >> 20} MiB write, untimed)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# the GB300 arm
+# ---------------------------------------------------------------------------
+
+def run_gb300(args):
+    import torch
+
+    from reduction_rdx_sum_gb300 import abi
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the library has no CPU path")
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    abi.load()
+    peak, peak_kind = load_peak()
+
+    arrays, distinct = suite_arrays()
+    dev_arrays = {}
+    for key, host in distinct.items():
+        t = torch.from_numpy(host.view(np.int16) if host.dtype == np.uint16 else host)
+        dev_arrays[key] = t.to(dev)
+    ops = []
+    for w in inputs.SUITE:
+        x = dev_arrays[(w.dist, w.seed, w.numel)]
+        if w.op == "rowsum_f32":
+            x = x.view(*w.shape)
+            out = torch.empty(w.shape[0], dtype=torch.float32, device=dev)
+            fn = abi.rdx_rowsum_f32
+        else:
+            out = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=dev)
+            fn = abi.SCALAR_OPS[w.op]
+        ops.append((w, fn, x, out))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(record):
+        for k, (w, fn, x, out) in enumerate(ops):
+            flush.zero_()
+            if record is not None:
+                record[k][0].record(stream)
+            fn(x, out=out, stream=stream)
+            if record is not None:
+                record[k][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops] for _ in range(args.steps)]
+    clocks_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None
+    with ClockSampler(local, clocks_path) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for s in range(args.steps):
+            one_step(events[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        barrier(world)
+    launch_ms = np.array([[e[0].elapsed_time(e[1]) for e in step] for step in events])  # (steps, ops)
+    device_s = float(launch_ms.sum()) / 1e3
+    device_s = max_over_ranks(world, device_s)
+    total_bytes = step_bytes() * args.steps * world
+    value = total_bytes / device_s / 1e9
+
+    per_config = {}
+    for k, (w, _, _, _) in enumerate(ops):
+        med = float(np.median(launch_ms[:, k]))
+        gbs = w.bytes_read / (med * 1e-3) / 1e9
+        per_config[w.name] = {"us": round(med * 1e3, 2), "GB/s": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4), "bytes": w.bytes_read}
+    shares = launch_ms.sum(axis=0) / launch_ms.sum()
+    top = int(np.argmax(shares))
+    wtop = ops[top][0]
+    achieved = wtop.bytes_read / (float(launch_ms[:, top].mean()) * 1e-3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(wtop.name)
+    traffic = traffic["bytes_per_launch"] if traffic and traffic.get("source_hash") == src_hash else None
+
+    # ---- ladder (the page's five block reductions) on the fp32 array --------
+    ladder = {}
+    x2 = dev_arrays[(inputs.CFG2_SUM_F32.dist, inputs.CFG2_SUM_F32.seed, inputs.CFG2_SUM_F32.numel)]
+    for v in range(1, 6):
+        part = torch.empty(abi.rdx_ladder_num_partials(v, x2.numel()), dtype=torch.float32, device=dev)
+        ts = []
+        for it in range(max(3, min(args.steps, 10)) + 2):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            abi.rdx_ladder_partials_f32(v, x2, out=part, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                ts.append(e0.elapsed_time(e1))
+        med = float(np.median(ts))
+        ladder[f"v{v}"] = {"us": round(med * 1e3, 2), "GB/s": round(x2.numel() * 4 / (med * 1e-3) / 1e9, 1)}
+
+    # ---- end to end from pinned host memory ----------------------------------
+    pinned = {}
+    for key, host in distinct.items():
+        t = torch.empty(host.size, dtype=dev_arrays[key].dtype, pin_memory=True)
+        t.numpy()[:] = host.view(np.int16) if host.dtype == np.uint16 else host
+        pinned[key] = t
+    outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for (_, _, _, o) in ops]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(o.numel() * o.element_size() for (_, _, _, o) in ops)
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        for key, t in pinned.items():
+            dev_arrays[key].copy_(t, non_blocking=True)
+        for (w, fn, x, out) in ops:
+            fn(x, out=out, stream=stream)
+        for (_, _, _, out), oh in zip(ops, outs_host):
+            oh.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(world, ea.elapsed_time(eb) / 1e3)
+    e2e_value = step_bytes() * e2e_steps * world / e2e_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(device_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32,i64",
+        "data": "synthetic", "config": config_block(),
+        "frac_of_peak": round(value / peak, 4),
+        "per_config": per_config,
+        "roofline": {"bound": "hbm", "kernel": wtop.name, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": wtop.bytes_read, "time_share": round(float(shares[top]), 4),
+                     "peak_source": f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": len(ops) * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+        "ladder_fp32_n2^24+13": ladder,
+        "kernel_source_hash": src_hash,
+    }
+    if rank == 0 and world == 1:
+        import oracle
+
+        oracle.build()
+        frac = calibrate_oracle(arrays, 12.0)
+        b, s = oracle_pass(arrays, frac)
+        line["cpu_baseline"] = {
+            "value": round(b / s / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {frac:.2%} of every workload of one step ({b / 1e6:.0f} MB), one thread, {s:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

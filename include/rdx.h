@@ -1,0 +1,159 @@
+/*
+ * rdx.h -- C ABI of the GB300 (sm_103a) parallel sum-reduction library
+ * (librdx.so).
+ *
+ * The operation is the parallel sum reduction of a large array worked through
+ * in the page "03_shared_memory_sync_reduction.py", demo 3 (parallel
+ * reduction): many threads cooperate to add up an array, each block
+ * producing one partial sum.  Here the partials are finished on the device in
+ * a fixed order, so every call returns the whole sum, and the result is
+ * bitwise reproducible from run to run on the same GPU model.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are device pointers (memory the current CUDA device can read
+ *    and write: cudaMalloc, torch CUDA tensors, managed memory).  The caller
+ *    owns the input and the output buffers.
+ *  - Every call is asynchronous: it validates its arguments, enqueues one
+ *    kernel on `stream` and returns.  The result is valid in stream order.
+ *    `stream` must belong to the current CUDA device; 0 is the legacy default
+ *    stream.
+ *  - Sizes are element counts (int64_t); no size limit beyond device memory.
+ *  - Any element-aligned input pointer is accepted; 16-byte alignment is not
+ *    required.  The output must not overlap the input.
+ *  - Scratch: the scalar reductions keep one small workspace per (device,
+ *    stream) pair (block partials and a completion counter), allocated by the
+ *    library with cudaMalloc on the first call on that pair and reused after.
+ *    Make that first call outside any CUDA-graph capture.  Two host threads
+ *    may call concurrently; calls on one stream are ordered by the stream.
+ *    rdx_shutdown() frees the workspaces.
+ *  - Errors: no exception crosses this ABI.  Each call returns an rdx_status;
+ *    argument errors are found before any CUDA call and nothing is enqueued.
+ *    After RDX_ERR_CUDA, rdx_last_cuda_error() names the failing CUDA call.
+ *
+ * Floating-point results
+ * ----------------------
+ * Float sums accumulate in float32 along a fixed tree (per-thread vector
+ * folds, a warp shuffle tree, a cross-warp stage, and a fixed-order pass over
+ * the block partials).  The order depends on n and on the GPU's SM count only,
+ * never on timing, so a repeated call gives the same bits.  Measured against
+ * the exact sum, the error stays within 1e-6 * sum|x_i| for float32 input and
+ * 4e-6 * sum|x_i| for bfloat16 input (sum of squares: the same factors times
+ * sum x_i^2).  Inf and NaN propagate as in an IEEE sum.
+ */
+#ifndef RDX_H
+#define RDX_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int rdx_status;
+
+#define RDX_OK 0                      /* enqueued (or nothing to do)                    */
+#define RDX_ERR_INVALID_ARG 1         /* bad pointer, size, alignment, overlap, version */
+#define RDX_ERR_CUDA 2                /* a CUDA runtime call or a launch failed         */
+#define RDX_ERR_ALLOC 3               /* the workspace could not be allocated           */
+#define RDX_ERR_UNSUPPORTED_DEVICE 4  /* the current device is not sm_103 (GB300)       */
+
+/* bfloat16 values are passed as their raw 16-bit patterns (the upper half of
+ * the IEEE binary32 with the same value). */
+typedef uint16_t rdx_bf16;
+
+/*
+ * rdx_sum_f32: *out = sum_{i<n} x[i].
+ * Page "03_shared_memory_sync_reduction.py", demo 3: the sum of a float32
+ * array (the page's expected value is this sum in float64).
+ *   x    n float32 values, contiguous, 4-byte aligned (NULL allowed if n == 0)
+ *   n    element count, >= 0; n == 0 writes 0.0f
+ *   out  one float32 in device memory
+ * Errors: RDX_ERR_INVALID_ARG if n < 0, out == NULL, x == NULL with n > 0,
+ * a pointer is not aligned to its element size, or out lies inside x.
+ */
+rdx_status rdx_sum_f32(const float* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_sumsq_f32: *out = sum_{i<n} x[i]^2, float32 accumulation.
+ * The same reduction with the square of each input as the term (the
+ * "one add per element" of the page becomes one multiply-add per element).
+ * Arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_sumsq_f32(const float* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_sum_bf16_f32acc: *out = sum_{i<n} x[i], bfloat16 input widened exactly
+ * to float32, float32 accumulation.  x is 2-byte aligned.
+ * Arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_sum_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_sumsq_bf16_f32acc: *out = sum_{i<n} x[i]^2, bfloat16 input, float32
+ * accumulation.  Arguments and errors as rdx_sum_bf16_f32acc.
+ */
+rdx_status rdx_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_sum_i32_i64: *out = sum_{i<n} x[i], int32 input, int64 accumulation.
+ * Integer addition is associative, so the result is exact and equal to the
+ * sequential sum bit for bit (no overflow for n < 2^32).  x 4-byte aligned,
+ * out 8-byte aligned.  Other arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_sum_i32_i64(const int32_t* x, int64_t n, int64_t* out, cudaStream_t stream);
+
+/*
+ * rdx_rowsum_f32: out[r] = sum_{j<cols} x[r*cols + j] for r < rows.
+ * The row-segmented sum: on the page each block of versions 1-3 writes the
+ * sum of B consecutive inputs (2B for versions 4-5) to out[blockIdx], i.e. a
+ * segmented sum with fixed-length segments; here a segment is a matrix row.
+ *   x     rows*cols float32 values, row-major and contiguous, 4-byte aligned
+ *   rows  >= 0; rows == 0 enqueues nothing
+ *   cols  >= 0; cols == 0 writes rows zeros
+ *   out   rows float32 values; must not overlap x
+ * Each row is summed by one group of threads in a fixed order, with no
+ * workspace and no cross-block step.
+ * Errors: RDX_ERR_INVALID_ARG for negative sizes, rows*cols overflowing
+ * int64, NULL or misaligned pointers, overlap.
+ */
+rdx_status rdx_rowsum_f32(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream);
+
+/*
+ * rdx_ladder_partials_f32: the page's five block-reduction versions, run as
+ * written (block of 256 threads), one float32 partial per block:
+ *   version 1  interleaved addressing, divergent branch (tid % 2s == 0)
+ *   version 2  interleaved addressing, consecutive threads (index = 2 s tid)
+ *   version 3  sequential addressing
+ *   version 4  first add during load (each block covers 512 inputs)
+ *   version 5  version 4 + warp shuffle for the last 32 values
+ * partials[b] = sum of the inputs block b covers (256 for versions 1-3, 512
+ * for 4-5), combined in that version's tree order; inputs past n count as 0.
+ *   partials  rdx_ladder_num_partials(version, n) float32 values
+ * This is the teaching ladder kept for comparison; rdx_sum_f32 is the fast
+ * path.  Errors: RDX_ERR_INVALID_ARG for a version outside 1..5, n < 0, NULL
+ * or misaligned pointers, overlap.
+ */
+rdx_status rdx_ladder_partials_f32(int version, const float* x, int64_t n, float* partials,
+                                   cudaStream_t stream);
+
+/* Number of partials rdx_ladder_partials_f32 writes: ceil(n / 256) for
+ * versions 1-3, ceil(n / 512) for 4-5; -1 for a bad version or n < 0. */
+int64_t rdx_ladder_num_partials(int version, int64_t n);
+
+/* Static text for a status code ("ok", "invalid argument", ...). */
+const char* rdx_status_string(rdx_status status);
+
+/* Text of the last CUDA error seen by an rdx call on this host thread
+ * ("" if none).  Valid until the next rdx call on the same thread. */
+const char* rdx_last_cuda_error(void);
+
+/* Free every cached workspace.  Call only when no rdx work is in flight. */
+void rdx_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RDX_H */

@@ -1,0 +1,189 @@
+"""Python binding of librdx.so: the C-ABI entry points under the same names.
+
+Argument marshalling only: each function checks the tensors it is given,
+passes their device pointers, sizes and the current CUDA stream to the C
+entry point, and raises ``RdxError`` on a non-zero status.  All arithmetic
+happens in the CUDA kernels.  If the library has not been built (see
+``reduction_rdx_sum_gb300.build``), every call raises; there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from .build import LIB
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rdx.h")
+
+RDX_OK = 0
+RDX_ERR_INVALID_ARG = 1
+RDX_ERR_CUDA = 2
+RDX_ERR_ALLOC = 3
+RDX_ERR_UNSUPPORTED_DEVICE = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RdxError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})" + (f": {detail}" if detail else ""))
+        self.status = status
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/rdx.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rdx_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str = LIB) -> ctypes.CDLL:
+    """Open librdx.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is not built; run reduction_rdx_sum_gb300.build.build() "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("rdx_sum_f32", "rdx_sumsq_f32", "rdx_sum_bf16_f32acc", "rdx_sumsq_bf16_f32acc",
+                     "rdx_sum_i32_i64"):
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = [vp, i64, vp, vp], i32
+        lib.rdx_rowsum_f32.argtypes, lib.rdx_rowsum_f32.restype = [vp, i64, i64, vp, vp], i32
+        lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
+        lib.rdx_ladder_partials_f32.restype = i32
+        lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
+        lib.rdx_status_string.argtypes, lib.rdx_status_string.restype = [i32], ctypes.c_char_p
+        lib.rdx_last_cuda_error.argtypes, lib.rdx_last_cuda_error.restype = [], ctypes.c_char_p
+        lib.rdx_shutdown.argtypes, lib.rdx_shutdown.restype = [], None
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().rdx_status_string(status).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != RDX_OK:
+        raise RdxError(fn, status, load().rdx_last_cuda_error().decode())
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _input(x: torch.Tensor, dtypes, what: str) -> torch.Tensor:
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise TypeError(f"{what}: expected a CUDA tensor")
+    if x.dtype not in dtypes:
+        raise TypeError(f"{what}: expected dtype in {dtypes}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    return x
+
+
+def _output(out, like: torch.Tensor, dtype, shape) -> torch.Tensor:
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    if not out.is_cuda or out.dtype != dtype or tuple(out.shape) != tuple(shape) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous CUDA {dtype} tensor of shape {tuple(shape)}")
+    return out
+
+
+def _scalar(name: str, x: torch.Tensor, dtypes, out_dtype, out, stream) -> torch.Tensor:
+    lib = load()
+    x = _input(x, dtypes, name)
+    out = _output(out, x, out_dtype, ())
+    with torch.cuda.device(x.device):
+        st = getattr(lib, name)(x.data_ptr(), x.numel(), out.data_ptr(), _stream_handle(stream, x.device))
+    _check(name, st)
+    return out
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+def rdx_sum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of a float32 tensor."""
+    return _scalar("rdx_sum_f32", x, (torch.float32,), torch.float32, out, stream)
+
+
+def rdx_sumsq_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of squares of a float32 tensor."""
+    return _scalar("rdx_sumsq_f32", x, (torch.float32,), torch.float32, out, stream)
+
+
+def rdx_sum_bf16_f32acc(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of a bfloat16 tensor (or its raw 16-bit patterns)."""
+    return _scalar("rdx_sum_bf16_f32acc", x, _BF16, torch.float32, out, stream)
+
+
+def rdx_sumsq_bf16_f32acc(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of squares of a bfloat16 tensor."""
+    return _scalar("rdx_sumsq_bf16_f32acc", x, _BF16, torch.float32, out, stream)
+
+
+def rdx_sum_i32_i64(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d int64 tensor: the exact sum of an int32 tensor."""
+    return _scalar("rdx_sum_i32_i64", x, (torch.int32,), torch.int64, out, stream)
+
+
+def rdx_rowsum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """(rows,) float32 tensor: per-row sums of a contiguous 2-D float32 tensor."""
+    lib = load()
+    x = _input(x, (torch.float32,), "rdx_rowsum_f32")
+    if x.dim() != 2:
+        raise ValueError("rdx_rowsum_f32: expected a 2-D tensor")
+    rows, cols = x.shape
+    out = _output(out, x, torch.float32, (rows,))
+    with torch.cuda.device(x.device):
+        st = lib.rdx_rowsum_f32(x.data_ptr(), rows, cols, out.data_ptr(), _stream_handle(stream, x.device))
+    _check("rdx_rowsum_f32", st)
+    return out
+
+
+def rdx_ladder_num_partials(version: int, n: int) -> int:
+    return int(load().rdx_ladder_num_partials(version, n))
+
+
+def rdx_ladder_partials_f32(version: int, x: torch.Tensor, out: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Per-block partials of the page's block-reduction ``version`` (1..5)."""
+    lib = load()
+    x = _input(x, (torch.float32,), "rdx_ladder_partials_f32")
+    nb = lib.rdx_ladder_num_partials(version, x.numel())
+    if nb < 0:
+        raise ValueError(f"rdx_ladder_partials_f32: bad version {version}")
+    out = _output(out, x, torch.float32, (nb,))
+    with torch.cuda.device(x.device):
+        st = lib.rdx_ladder_partials_f32(version, x.data_ptr(), x.numel(), out.data_ptr(),
+                                         _stream_handle(stream, x.device))
+    _check("rdx_ladder_partials_f32", st)
+    return out
+
+
+def rdx_shutdown() -> None:
+    load().rdx_shutdown()
+
+
+# Entry points by operation name, for the tests and the bench.
+SCALAR_OPS = {
+    "sum_f32": rdx_sum_f32,
+    "sumsq_f32": rdx_sumsq_f32,
+    "sum_bf16": rdx_sum_bf16_f32acc,
+    "sumsq_bf16": rdx_sumsq_bf16_f32acc,
+    "sum_i32": rdx_sum_i32_i64,
+}

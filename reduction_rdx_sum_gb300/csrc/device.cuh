@@ -1,0 +1,159 @@
+// device.cuh -- device-side building blocks shared by the reduction kernels:
+// streaming 16-byte loads, the per-dtype "fold" of one 16-byte vector, the
+// warp shuffle tree and the two-level block tree.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rdx {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kWarpSize = 32;
+
+// One 16-byte load on the read-only path.  Every input byte is read once, so
+// the line is not kept in L1 (L1::no_allocate); L2::256B asks the L2 to fetch
+// the whole 256-byte span the warp is about to stream through.  The asm is
+// volatile so that a batch of these loads keeps its program order.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Issue order fence for a batch of loads: every register of v passes through
+// an empty volatile asm placed after the whole batch, so no arithmetic on the
+// batch can be scheduled between its loads and all N loads are in flight
+// together (the compiler would otherwise sink each load next to its use).
+template <int N>
+__device__ __forceinline__ void batch_fence(uint4 (&v)[N]) {
+#pragma unroll
+    for (int u = 0; u < N; ++u) asm volatile("" : "+r"(v[u].x), "+r"(v[u].y), "+r"(v[u].z), "+r"(v[u].w));
+}
+
+// ---------------------------------------------------------------------------
+// Term policies.  Each describes one reduction: the input element type, the
+// accumulator, how one element becomes a term, and how the 16-byte vector of
+// V elements becomes one accumulator value (a fixed pairwise tree, so every
+// run adds the same operands in the same order).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+struct SumF32 {
+    using In = float;
+    using Acc = float;
+    static constexpr int kVec = 4;
+    __device__ static Acc term(In v) { return v; }
+    __device__ static Acc fold(uint4 v) {
+        return (__uint_as_float(v.x) + __uint_as_float(v.y)) + (__uint_as_float(v.z) + __uint_as_float(v.w));
+    }
+};
+
+struct SumSqF32 {
+    using In = float;
+    using Acc = float;
+    static constexpr int kVec = 4;
+    __device__ static Acc term(In v) { return v * v; }
+    __device__ static Acc fold(uint4 v) {
+        const float a = __uint_as_float(v.x), b = __uint_as_float(v.y);
+        const float c = __uint_as_float(v.z), d = __uint_as_float(v.w);
+        return __fmaf_rn(a, a, b * b) + __fmaf_rn(c, c, d * d);
+    }
+};
+
+struct SumBF16 {
+    using In = uint16_t;
+    using Acc = float;
+    static constexpr int kVec = 8;
+    __device__ static Acc term(In v) { return __uint_as_float(uint32_t(v) << 16); }
+    __device__ static float pair(uint32_t w) { return bf16_lo(w) + bf16_hi(w); }
+    __device__ static Acc fold(uint4 v) { return (pair(v.x) + pair(v.y)) + (pair(v.z) + pair(v.w)); }
+};
+
+struct SumSqBF16 {
+    using In = uint16_t;
+    using Acc = float;
+    static constexpr int kVec = 8;
+    __device__ static Acc term(In v) {
+        const float f = __uint_as_float(uint32_t(v) << 16);
+        return f * f;
+    }
+    __device__ static float pair(uint32_t w) {
+        const float lo = bf16_lo(w), hi = bf16_hi(w);
+        return __fmaf_rn(lo, lo, hi * hi);
+    }
+    __device__ static Acc fold(uint4 v) { return (pair(v.x) + pair(v.y)) + (pair(v.z) + pair(v.w)); }
+};
+
+struct SumI32 {
+    using In = int32_t;
+    using Acc = long long;
+    static constexpr int kVec = 4;
+    __device__ static Acc term(In v) { return Acc(v); }
+    __device__ static Acc fold(uint4 v) {
+        return (Acc(int32_t(v.x)) + Acc(int32_t(v.y))) + (Acc(int32_t(v.z)) + Acc(int32_t(v.w)));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Trees.
+// ---------------------------------------------------------------------------
+
+// Lane 0 ends with the sum of the 32 lanes' values: shuffle-down by 16, 8, 4,
+// 2, 1 (lanes past the warp's end read their own value, which never reaches
+// lane 0).
+template <class T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int off = kWarpSize / 2; off > 0; off >>= 1) v += __shfl_down_sync(kFullMask, v, off);
+    return v;
+}
+
+// Every lane of each aligned group of `width` lanes ends with the group's sum.
+// In the xor butterfly both partners add the same two values, so all lanes of
+// the group hold the identical result.
+template <int width, class T>
+__device__ __forceinline__ T group_allreduce(T v) {
+#pragma unroll
+    for (int off = width / 2; off > 0; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+    return v;
+}
+
+// Fixed pairwise fold of a register array (N a power of two).
+template <int N, class T>
+__device__ __forceinline__ T fold_array(T (&a)[N]) {
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) a[i] = a[i] + a[i + w];
+    }
+    return a[0];
+}
+
+// Block tree: warp trees, then lane 0 of warp w parks its value in smem[w]
+// and warp 0 reduces smem[0 .. kWarps) (consecutive words: one shared-memory
+// wavefront, no bank conflict).  The result is valid in thread 0.  smem must
+// not be in use by other threads when called; the call ends before any
+// thread may write smem again only after a later __syncthreads().
+template <int kBlock, class T>
+__device__ __forceinline__ T block_sum(T v, T* smem) {
+    constexpr int kWarps = kBlock / kWarpSize;
+    static_assert(kWarps <= kWarpSize, "block too large for a one-warp second stage");
+    v = warp_sum(v);
+    const int lane = threadIdx.x % kWarpSize;
+    const int warp = threadIdx.x / kWarpSize;
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    T r = T(0);
+    if (warp == 0) {
+        r = lane < kWarps ? smem[lane] : T(0);
+        r = warp_sum(r);
+    }
+    return r;
+}
+
+}  // namespace rdx

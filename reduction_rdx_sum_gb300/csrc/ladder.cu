@@ -1,0 +1,97 @@
+// ladder.cu -- the five block-level reductions of the page
+// "03_shared_memory_sync_reduction.py", demo 3 (after Harris, "Optimizing
+// Parallel Reduction in CUDA", 2007), as real CUDA kernels with the page's
+// block of B = 256 threads and one float32 partial per block.
+//
+//   version 1  interleaved addressing: at step s the threads with
+//              tid % 2s == 0 add sdata[tid + s] into sdata[tid]  (divergent)
+//   version 2  interleaved addressing by consecutive threads:
+//              index = 2 s tid, sdata[index] += sdata[index + s]  (bank
+//              conflicts: stride 2s words)
+//   version 3  sequential addressing: for s = B/2 .. 1 the first s threads
+//              add sdata[tid + s] into sdata[tid]
+//   version 4  version 3 with the first add during load: a block covers 2B
+//              inputs, thread tid loads in[i] + in[i + B]
+//   version 5  version 4, the shared-memory loop stopped at 64, then warp 0
+//              adds sdata[tid] + sdata[tid + 32] and finishes with
+//              __shfl_down_sync by 16, 8, 4, 2, 1
+//
+// They are kept as the comparison ladder for the fast kernel in reduce.cu.
+// The page launches n / (B * per_thread) blocks and reads no index past the
+// end; here the last block may be partial and inputs past n count as 0.
+#include "device.cuh"
+#include "launch.h"
+
+namespace rdx {
+namespace {
+
+constexpr int B = kLadderBlock;
+
+template <int V>
+__global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in, int64_t n,
+                                                   float* __restrict__ out) {
+    __shared__ float sdata[B];
+    const int tid = threadIdx.x;
+    const int64_t bx = blockIdx.x;
+
+    if (V <= 3) {
+        const int64_t i = bx * B + tid;
+        sdata[tid] = i < n ? in[i] : 0.f;
+    } else {
+        const int64_t i = bx * (2 * B) + tid;
+        const float a = i < n ? in[i] : 0.f;
+        const float b = i + B < n ? in[i + B] : 0.f;
+        sdata[tid] = a + b;
+    }
+    __syncthreads();
+
+    if (V == 1) {
+        for (int s = 1; s < B; s *= 2) {
+            if (tid % (2 * s) == 0) sdata[tid] += sdata[tid + s];
+            __syncthreads();
+        }
+    } else if (V == 2) {
+        for (int s = 1; s < B; s *= 2) {
+            const int index = 2 * s * tid;
+            if (index < B) sdata[index] += sdata[index + s];
+            __syncthreads();
+        }
+    } else if (V == 3 || V == 4) {
+        for (int s = B / 2; s > 0; s >>= 1) {
+            if (tid < s) sdata[tid] += sdata[tid + s];
+            __syncthreads();
+        }
+    } else {
+        for (int s = B / 2; s >= 64; s >>= 1) {
+            if (tid < s) sdata[tid] += sdata[tid + s];
+            __syncthreads();
+        }
+        if (tid < kWarpSize) {
+            float val = sdata[tid] + sdata[tid + 32];
+            for (int off = 16; off > 0; off >>= 1) val += __shfl_down_sync(kFullMask, val, off);
+            if (tid == 0) out[bx] = val;
+        }
+        return;
+    }
+    if (tid == 0) out[bx] = sdata[0];
+}
+
+}  // namespace
+
+cudaError_t ladder_launch(int version, const float* x, int64_t n, float* partials, int64_t blocks,
+                          cudaStream_t stream) {
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const unsigned g = unsigned(blocks);
+    switch (version) {
+        case 1: ladder_kernel<1><<<g, B, 0, stream>>>(x, n, partials); break;
+        case 2: ladder_kernel<2><<<g, B, 0, stream>>>(x, n, partials); break;
+        case 3: ladder_kernel<3><<<g, B, 0, stream>>>(x, n, partials); break;
+        case 4: ladder_kernel<4><<<g, B, 0, stream>>>(x, n, partials); break;
+        case 5: ladder_kernel<5><<<g, B, 0, stream>>>(x, n, partials); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace rdx

@@ -1,0 +1,93 @@
+"""The C-ABI library on the host, without a GPU: it builds for sm_103a, loads,
+exports every function include/rdx.h declares, and rejects bad arguments
+before making any CUDA call."""
+import ctypes
+import os
+
+import pytest
+
+from reduction_rdx_sum_gb300 import abi, build
+
+INVALID = abi.RDX_ERR_INVALID_ARG
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = abi.declared_symbols()
+    assert {"rdx_sum_f32", "rdx_sum_bf16_f32acc", "rdx_sum_i32_i64", "rdx_rowsum_f32",
+            "rdx_sumsq_f32"} <= set(names)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_is_in_tree_and_for_sm103a(lib):
+    assert os.path.dirname(build.LIB) == os.path.dirname(abi.__file__)
+    assert any("arch=compute_103a,code=sm_103a" == f for f in build.NVCC_FLAGS)
+
+
+def test_status_strings(lib):
+    assert abi.status_string(0) == "ok"
+    assert abi.status_string(INVALID) == "invalid argument"
+    assert "allocation" in abi.status_string(abi.RDX_ERR_ALLOC)
+    assert abi.status_string(99) == "unknown status"
+    assert lib.rdx_last_cuda_error() == b""
+
+
+# Argument errors are detected before any CUDA runtime call, so these run
+# without a GPU.  A fake device address is fine: nothing dereferences it.
+FAKE = 1 << 40
+
+
+@pytest.mark.parametrize("name,esize,osize", [
+    ("rdx_sum_f32", 4, 4), ("rdx_sumsq_f32", 4, 4), ("rdx_sum_bf16_f32acc", 2, 4),
+    ("rdx_sumsq_bf16_f32acc", 2, 4), ("rdx_sum_i32_i64", 4, 8)])
+def test_scalar_argument_validation(lib, name, esize, osize):
+    fn = getattr(lib, name)
+    assert fn(FAKE, -1, FAKE + 4096, None) == INVALID                 # negative n
+    assert fn(FAKE, 10, None, None) == INVALID                         # no output
+    assert fn(None, 10, FAKE, None) == INVALID                         # no input
+    assert fn(FAKE + 1, 10, FAKE + 4096, None) == INVALID              # input not element-aligned
+    assert fn(FAKE, 10, FAKE + 4096 + osize // 2, None) == INVALID     # output misaligned
+    assert fn(FAKE, 10, FAKE + esize * 3, None) == INVALID             # output inside the input
+    assert fn(FAKE, 10, FAKE + esize * 10 - osize, None) == INVALID    # output on the last element
+    assert fn(FAKE, 1 << 62, FAKE - 64, None) == INVALID              # size overflow
+
+
+def test_rowsum_argument_validation(lib):
+    f = lib.rdx_rowsum_f32
+    assert f(FAKE, -1, 4, FAKE + 4096, None) == INVALID
+    assert f(FAKE, 4, -1, FAKE + 4096, None) == INVALID
+    assert f(FAKE, 4, 4, None, None) == INVALID
+    assert f(None, 4, 4, FAKE, None) == INVALID
+    assert f(FAKE + 2, 4, 4, FAKE + 4096, None) == INVALID
+    assert f(FAKE, 4, 4, FAKE + 32, None) == INVALID                  # out overlaps x
+    assert f(FAKE, 1 << 40, 1 << 40, FAKE - 64, None) == INVALID      # rows*cols overflows
+    assert f(None, 0, 5, None, None) == abi.RDX_OK                     # nothing to do
+
+
+def test_ladder_argument_validation(lib):
+    f = lib.rdx_ladder_partials_f32
+    assert f(0, FAKE, 10, FAKE + 4096, None) == INVALID
+    assert f(6, FAKE, 10, FAKE + 4096, None) == INVALID
+    assert f(3, FAKE, -5, FAKE + 4096, None) == INVALID
+    assert f(3, None, 10, FAKE, None) == INVALID
+    assert f(3, FAKE, 1000, FAKE + 512, None) == INVALID              # partials inside x
+    assert f(3, None, 0, None, None) == abi.RDX_OK
+    n = lib.rdx_ladder_num_partials
+    assert [n(v, 0) for v in range(1, 6)] == [0] * 5
+    assert [n(v, 1) for v in range(1, 6)] == [1] * 5
+    assert [n(v, 256) for v in range(1, 6)] == [1, 1, 1, 1, 1]
+    assert [n(v, 257) for v in range(1, 6)] == [2, 2, 2, 1, 1]
+    assert [n(v, 1 << 18) for v in range(1, 6)] == [1024, 1024, 1024, 512, 512]
+    assert n(0, 5) == -1 and n(1, -1) == -1
+
+
+def test_python_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        abi.load(str(tmp_path / "missing.so"))

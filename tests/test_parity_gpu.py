@@ -1,0 +1,325 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: integer sums bit-exact; float32 input |gpu - oracle| <= 1e-6 * sum|x_i|
++ 1e-30; bfloat16 input 4e-6 * sum|x_i|; sums of squares the same factors
+times sum x_i^2; row sums per row against that row's sum |x|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from reduction_rdx_sum_gb300 import abi, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+FACTOR = {"sum_f32": 1e-6, "sumsq_f32": 1e-6, "sum_bf16": 4e-6, "sumsq_bf16": 4e-6}
+OPS = ["sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32"]
+VEC = {"sum_f32": 4, "sumsq_f32": 4, "sum_bf16": 8, "sumsq_bf16": 8, "sum_i32": 4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from reduction_rdx_sum_gb300 import build
+
+    build.build()
+    oracle.build()
+    abi.load()
+    torch.cuda.set_device(DEV)
+
+
+def host_input(op, n, seed):
+    if op in ("sum_f32", "sumsq_f32"):
+        return inputs.normal_f32(n, seed)
+    if op in ("sum_bf16", "sumsq_bf16"):
+        return inputs.normal_bf16_bits(n, seed)
+    return inputs.integers_i32(n, seed, -(2 ** 31), 2 ** 31 - 1)  # full range: int64 carries
+
+
+def to_device(host, offset=0):
+    """Device copy of host; with offset > 0 the returned view starts offset
+    elements into an allocation (its address is misaligned by that much)."""
+    a = host.view(np.int16) if host.dtype == np.uint16 else host
+    buf = torch.empty(a.size + offset, dtype=torch.from_numpy(a[:0]).dtype, device=DEV)
+    view = buf[offset:]
+    view.copy_(torch.from_numpy(a))
+    return view
+
+
+def reference(op, host):
+    """(oracle value, tolerance) for a scalar op."""
+    if op == "sum_i32":
+        return oracle.sum_i32(host), 0
+    if op == "sum_f32":
+        return oracle.sum_f32(host), FACTOR[op] * oracle.abssum_f32(host) + 1e-30
+    if op == "sumsq_f32":
+        v = oracle.sumsq_f32(host)
+        return v, FACTOR[op] * v + 1e-30
+    if op == "sum_bf16":
+        return oracle.sum_bf16(host), FACTOR[op] * oracle.abssum_bf16(host) + 1e-30
+    v = oracle.sumsq_bf16(host)
+    return v, FACTOR[op] * v + 1e-30
+
+
+def check(op, host, got):
+    ref, tol = reference(op, host)
+    if op == "sum_i32":
+        assert int(got) == ref
+    else:
+        assert abs(float(got) - ref) <= tol, (float(got), ref, tol)
+
+
+SIZES = [0, 1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511,
+         512, 513, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8193, 65535, 65536, 65537,
+         262143, 262144, 262145, (1 << 20) - 1, 1 << 20, (1 << 20) + 1, 1_000_003, (1 << 22) + 13,
+         (1 << 24) + 13]
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("n", SIZES)
+def test_scalar_parity(op, n):
+    host = host_input(op, n, seed=n % 97)
+    got = abi.SCALAR_OPS[op](to_device(host)).item()
+    check(op, host, got)
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("n", [1, 3, 5, 9, 100, 4097, (1 << 20) + 3])
+def test_scalar_parity_misaligned_base(op, n):
+    host = host_input(op, n, seed=7)
+    for offset in range(1, VEC[op]):
+        got = abi.SCALAR_OPS[op](to_device(host, offset)).item()
+        check(op, host, got)
+
+
+def test_empty_input_writes_zero():
+    for op in OPS:
+        dt = {"sum_f32": torch.float32, "sumsq_f32": torch.float32, "sum_bf16": torch.bfloat16,
+              "sumsq_bf16": torch.bfloat16, "sum_i32": torch.int32}[op]
+        out = torch.full((), 123, dtype=torch.int64 if op == "sum_i32" else torch.float32, device=DEV)
+        abi.SCALAR_OPS[op](torch.empty(0, dtype=dt, device=DEV), out=out)
+        assert out.item() == 0
+
+
+def test_page_worked_example_sum():
+    # "03_shared_memory_sync_reduction.py", demo 3: in[i] = i mod 7, exact sums
+    for n, total in ((1 << 14, 49146), (1 << 18, 786429)):
+        x = torch.from_numpy((np.arange(n) % 7).astype(np.float32)).to(DEV)
+        assert abi.rdx_sum_f32(x).item() == total
+
+
+def test_integer_extremes_exact():
+    n = (1 << 24) + 5
+    for v in (2 ** 31 - 1, -(2 ** 31)):
+        x = torch.full((n,), v, dtype=torch.int32, device=DEV)
+        assert abi.rdx_sum_i32_i64(x).item() == v * n
+
+
+def test_nonfinite_propagation():
+    n = 100_003
+    for pos in (0, 5, n // 2, n - 1):
+        x = torch.ones(n, dtype=torch.float32, device=DEV)
+        x[pos] = math.inf
+        assert abi.rdx_sum_f32(x).item() == math.inf
+        assert abi.rdx_sumsq_f32(x).item() == math.inf
+        x[(pos + 7) % n] = -math.inf
+        assert math.isnan(abi.rdx_sum_f32(x).item())
+        x = torch.ones(n, dtype=torch.float32, device=DEV)
+        x[pos] = math.nan
+        assert math.isnan(abi.rdx_sum_f32(x).item())
+        b = torch.ones(n, dtype=torch.bfloat16, device=DEV)
+        b[pos] = -math.inf
+        assert abi.rdx_sum_bf16_f32acc(b).item() == -math.inf
+
+
+# ---------------------------------------------------------------------------
+# the five workload configurations at full size
+# ---------------------------------------------------------------------------
+
+_cache = {}
+
+
+def workload(w):
+    if w.name not in _cache:
+        _cache.clear()
+        _cache[w.name] = inputs.make(w)
+    return _cache[w.name]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", inputs.SMALL + (inputs.CFG2_SUM_F32, inputs.CFG2_SUMSQ_F32, inputs.CFG3_SUM_I32,
+                                              inputs.CFG5_SUM_BF16, inputs.CFG5_SUMSQ_BF16),
+                         ids=lambda w: w.name)
+def test_config_scalar(w):
+    host = workload(w)
+    got = abi.SCALAR_OPS[w.op](to_device(host)).item()
+    check(w.op, host, got)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", (inputs.CFG4_ROWSUM_WIDE, inputs.CFG4_ROWSUM_SKINNY), ids=lambda w: w.name)
+def test_config_rowsum(w):
+    host = workload(w)
+    got = abi.rdx_rowsum_f32(torch.from_numpy(host).to(DEV)).cpu().numpy().astype(np.float64)
+    ref = oracle.rowsum_f32(host)
+    tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+    bad = np.nonzero(~(np.abs(got - ref) <= tol))[0]
+    assert bad.size == 0, (bad[:5], got[bad[:5]], ref[bad[:5]])
+
+
+# ---------------------------------------------------------------------------
+# row-segmented sum
+# ---------------------------------------------------------------------------
+
+SHAPES = [(1, 1), (1, 3), (1, 1000), (3, 5), (7, 3), (31, 4), (33, 8), (33, 255), (100, 16), (100, 33),
+          (1000, 256), (1000, 257), (513, 64), (64, 1023), (64, 1024), (64, 1025), (17, 2048), (17, 4099),
+          (8, 100_000), (2, 1 << 20), (4097, 128), (50_000, 7), (1, 1 << 22)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=str)
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_rowsum_parity(shape, offset):
+    rows, cols = shape
+    host = inputs.uniform_f32(rows * cols, seed=rows + cols, lo=-1.0, hi=1.0).reshape(rows, cols)
+    x = to_device(host.reshape(-1), offset).view(rows, cols)
+    got = abi.rdx_rowsum_f32(x).cpu().numpy().astype(np.float64)
+    ref = oracle.rowsum_f32(host)
+    tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+    assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_rowsum_degenerate_shapes():
+    out = torch.full((5,), 7.0, device=DEV)
+    abi.rdx_rowsum_f32(torch.empty((5, 0), device=DEV), out=out)
+    assert out.tolist() == [0.0] * 5
+    assert abi.rdx_rowsum_f32(torch.empty((0, 9), device=DEV)).shape == (0,)
+
+
+def test_rowsum_page_segments():
+    # demo 3's per-block outputs are segment sums: B = 256 and 2B = 512
+    n = 1 << 18
+    x = (np.arange(n) % 7).astype(np.float32)
+    period = {256: [762, 771, 766, 768, 770, 765, 774], 512: [1533, 1534, 1535, 1536, 1537, 1538, 1539]}
+    for seg, p in period.items():
+        got = abi.rdx_rowsum_f32(torch.from_numpy(x.reshape(-1, seg)).to(DEV)).cpu().tolist()
+        assert got == [p[b % 7] for b in range(n // seg)]
+
+
+# ---------------------------------------------------------------------------
+# the page's five block reductions: bit-exact against the oracle's restatement
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("version", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("n", [1, 255, 256, 257, 511, 512, 513, 1 << 14, 1 << 18, (1 << 20) + 77])
+def test_ladder_bit_exact(version, n):
+    host = inputs.normal_f32(n, seed=version)
+    got = abi.rdx_ladder_partials_f32(version, torch.from_numpy(host).to(DEV)).cpu().numpy()
+    ref = oracle.ladder_partials(version, host)
+    assert got.shape == ref.shape
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("version", [1, 2, 3, 4, 5])
+def test_ladder_page_worked_example(version):
+    for n in (1 << 14, 1 << 18):
+        host = (np.arange(n) % 7).astype(np.float32)
+        got = abi.rdx_ladder_partials_f32(version, torch.from_numpy(host).to(DEV)).cpu().numpy()
+        assert np.array_equal(got, oracle.ladder_partials(version, host))
+        assert float(got.astype(np.float64).sum()) == {1 << 14: 49146, 1 << 18: 786429}[n]
+
+
+# ---------------------------------------------------------------------------
+# determinism, concurrency, limits, errors
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("op", OPS)
+def test_bitwise_deterministic(op):
+    x = to_device(host_input(op, (1 << 24) + 13, seed=1))
+    fn = abi.SCALAR_OPS[op]
+    first = fn(x).clone()
+    side = torch.cuda.Stream()
+    for i in range(10):
+        if i % 2:
+            with torch.cuda.stream(side):
+                got = fn(x, stream=side)
+            side.synchronize()
+        else:
+            got = fn(x)
+        assert torch.equal(got.view(torch.int32 if got.dtype == torch.float32 else torch.int64),
+                           first.view(torch.int32 if first.dtype == torch.float32 else torch.int64))
+
+
+def test_rowsum_deterministic():
+    for shape in ((8192, 4096), (1 << 16, 256)):
+        x = torch.rand(shape, device=DEV) * 2 - 1
+        a = abi.rdx_rowsum_f32(x)
+        for _ in range(5):
+            assert torch.equal(abi.rdx_rowsum_f32(x).view(torch.int32), a.view(torch.int32))
+
+
+def test_concurrent_streams():
+    hosts = [inputs.normal_f32((1 << 22) + i, seed=10 + i) for i in range(4)]
+    devs = [torch.from_numpy(h).to(DEV) for h in hosts]
+    streams = [torch.cuda.Stream() for _ in hosts]
+    outs = []
+    for _ in range(3):
+        outs = []
+        for x, s in zip(devs, streams):
+            with torch.cuda.stream(s):
+                outs.append(abi.rdx_sum_f32(x, stream=s))
+        torch.cuda.synchronize()
+    for h, o in zip(hosts, outs):
+        check("sum_f32", h, o.item())
+
+
+@pytest.mark.slow
+def test_largest_sizes_index_math():
+    # more than 2^31 elements (int32 and float32, 8 GiB) and more than 2^32
+    # bfloat16 elements (8 GiB): all ones, so the sum is n
+    n = (1 << 31) + 5
+    x = torch.ones(n, dtype=torch.int32, device=DEV)
+    assert abi.rdx_sum_i32_i64(x).item() == n
+    x = x.view(torch.float32).fill_(1.0)
+    assert abs(abi.rdx_sum_f32(x).item() - n) <= 1e-6 * n
+    del x
+    torch.cuda.empty_cache()
+    n = (1 << 32) + 3
+    b = torch.ones(n, dtype=torch.bfloat16, device=DEV)
+    assert abs(abi.rdx_sum_bf16_f32acc(b).item() - n) <= 4e-6 * n
+    del b
+    torch.cuda.empty_cache()
+
+
+def test_workspace_allocation_failure_is_reported(monkeypatch):
+    x = torch.ones(1 << 22, device=DEV)
+    fresh = torch.cuda.Stream()
+    monkeypatch.setenv("RDX_FAULT_ALLOC", "1")
+    with pytest.raises(abi.RdxError) as e:
+        abi.rdx_sum_f32(x, stream=fresh)
+    assert e.value.status == abi.RDX_ERR_ALLOC
+    # a one-block launch needs no workspace
+    small = abi.rdx_sum_f32(x[:100], stream=fresh)
+    fresh.synchronize()
+    assert small.item() == 100.0
+    monkeypatch.delenv("RDX_FAULT_ALLOC")
+    with torch.cuda.stream(fresh):
+        got = abi.rdx_sum_f32(x, stream=fresh)
+    fresh.synchronize()
+    assert got.item() == float(1 << 22)
+
+
+def test_overlap_and_bad_tensors_rejected():
+    x = torch.ones(1000, device=DEV)
+    with pytest.raises(abi.RdxError) as e:
+        abi.rdx_sum_f32(x[1:], out=x[500])
+    assert e.value.status == abi.RDX_ERR_INVALID_ARG
+    with pytest.raises(TypeError):
+        abi.rdx_sum_f32(x.double())
+    with pytest.raises(TypeError):
+        abi.rdx_sum_f32(torch.ones(10))
+    with pytest.raises(ValueError):
+        abi.rdx_sum_f32(torch.ones(10, 10, device=DEV).t())
+    assert abi.rdx_sum_f32(x).item() == 1000.0

@@ -142,6 +142,34 @@ rdx_status rdx_ladder_partials_f32(int version, const float* x, int64_t n, float
  * versions 1-3, ceil(n / 512) for 4-5; -1 for a bad version or n < 0. */
 int64_t rdx_ladder_num_partials(int version, int64_t n);
 
+/*
+ * rdx_sum_f32_noalloc: *out = sum_{i<n} x[i], like rdx_sum_f32, but the call
+ * allocates no device memory.  (The surveyed pages have no counterpart: this
+ * entry point exists for callers of this library, not for the method.)
+ *
+ * For callers that may not cudaMalloc while they run: code inside a framework
+ * whose allocator owns all device memory (an allocation behind its back is
+ * not accounted for and can fail once the framework has reserved the memory),
+ * latency-critical code (cudaMalloc/cudaFree may synchronize the device and
+ * cost far more than the sum), and programs whose memory budget is fixed at
+ * start-up.
+ *
+ * Same kernel, grid and summation order as rdx_sum_f32, so the same result.
+ * Scratch (block partials and a completion counter) lives in one static
+ * device array of 16 KiB + 256 B that every GPU loading this library holds
+ * until the process exits.  Limit: 4096 block partials; a launch that would
+ * need more (a device with more SMs than this library was sized for) is
+ * refused with RDX_ERR_INVALID_ARG and a message in rdx_last_cuda_error().
+ * All calls share the array and it keeps the last call's contents; the
+ * counter is cleared on `stream` before every launch.  Calls whose kernels
+ * overlap on the GPU (unordered streams) race on the array: order them.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * Arguments and other errors as rdx_sum_f32.
+ */
+rdx_status rdx_sum_f32_noalloc(const float* x, int64_t n, float* out, cudaStream_t stream);
+
 /* Static text for a status code ("ok", "invalid argument", ...). */
 const char* rdx_status_string(rdx_status status);
 

@@ -175,6 +175,16 @@ def rdx_ladder_partials_f32(version: int, x: torch.Tensor, out: torch.Tensor | N
     return out
 
 
+def rdx_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of a float32 tensor, computed with the
+    library's static scratch instead of an allocated workspace (for callers
+    that may not allocate device memory; calls must not overlap on the GPU)."""
+    lib = load()
+    fn = lib.rdx_sum_f32_noalloc
+    fn.argtypes, fn.restype = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int
+    return _scalar("rdx_sum_f32_noalloc", x, (torch.float32,), torch.float32, out, stream)
+
+
 def rdx_shutdown() -> None:
     load().rdx_shutdown()
 

@@ -137,6 +137,8 @@ rdx_status reduce_entry(Op op, const void* x, int64_t n, void* out, cudaStream_t
 
 }  // namespace
 
+void rdx::set_last_error(const char* text) { t_last_error = text; }
+
 extern "C" {
 
 rdx_status rdx_sum_f32(const float* x, int64_t n, float* out, cudaStream_t stream) {

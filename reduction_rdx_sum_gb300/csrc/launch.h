@@ -44,6 +44,10 @@ cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* warp_bps);
 cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
                           cudaStream_t stream);
 
+// ---- error text shared by every entry point (api.cu) ------------------------
+// Replace the calling thread's rdx_last_cuda_error() text.
+void set_last_error(const char* text);
+
 // ---- the page's five block reductions (ladder.cu) --------------------------
 constexpr int kLadderBlock = 256;
 cudaError_t ladder_launch(int version, const float* x, int64_t n, float* partials, int64_t blocks,

@@ -10,8 +10,9 @@ A step is one pass of every reduction entry point over its workload's input:
   bf16 -> fp32 sum and sum of squares of n = 2^30 + 7 normal(0,1) (seed 4).
 The metric is GB/s of input read by the reductions (algorithmic bytes / device
 time).  Every launch is timed with CUDA events on the stream it runs on, after
-an untimed 512 MiB write that flushes the L2 (129 MB), so each launch reads its
-input from HBM.  ``e2e`` repeats the step from pinned host memory: the
+an untimed L2 flush (a 512 MiB write, then a 512 MiB read so that the timed
+kernel finds no dirty line to write back), so each launch reads its input from
+HBM.  ``e2e`` repeats the step from pinned host memory: the
 host-to-device copies of the inputs and the device-to-host copies of the
 results are inside its timed region.  ``cpu_baseline`` times the CPU oracle
 (one core) on a bounded sample of the same step.
@@ -25,7 +26,6 @@ no collective on the data path); the time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -46,18 +46,34 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel from one ncu capture, and the hash of the kernel sources it was taken
-# on; reported as null once the sources differ.
-NCU_TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
+# (profiles/ has the summaries), with the source files that define the kernel
+# and their hash at capture time: a figure is reported only while those files
+# are unchanged.  The captures ran on n = 2^28 and are scaled to the full launch
+# by the element count (traffic grows in proportion).
+NCU_TRAFFIC = {
+    "c5_sum_bf16": {"bytes_per_launch": 2160926734, "sources": ("device.cuh", "reduce.cu"),
+                    "source_hash": "ff7c06a006ddd0e2",
+                    "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """Hash of the kernel sources (all of csrc/, or the named files)."""
+    csrc = os.path.join(ROOT, "reduction_rdx_sum_gb300", "csrc")
+    names = sorted(files) if files else sorted(os.listdir(csrc))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "reduction_rdx_sum_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    t = NCU_TRAFFIC.get(workload)
+    if t and kernel_source_hash(t["sources"]) == t["source_hash"]:
+        return t["bytes_per_launch"]
+    return None
 
 
 def load_peak():
@@ -221,7 +237,9 @@ def run_reference(args):
 
     oracle.build()
     arrays, _ = suite_arrays()
+    # about 150 s of oracle work for the whole run, at most 10 s per step
     per_step_budget = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step_budget = float(os.environ.get("RDX_BENCH_REFERENCE_BUDGET_S", per_step_budget))
     frac = calibrate_oracle(arrays, per_step_budget)
     for _ in range(args.warmup):
         oracle_pass(arrays, frac)
@@ -250,7 +268,8 @@ def config_block():
                     "fp32 rowsum 8192x32768 and 1048576x256 U[-1,1) s3; bf16->fp32 sum+sumsq n=2^30+7 N(0,1) s4",
         "bytes_read_per_step": step_bytes(),
         "launches_per_step": len(inputs.SUITE),
-        "l2": f"flushed before every timed launch ({FLUSH_BYTES >> 20} MiB write, untimed)",
+        "l2": f"flushed before every timed launch ({FLUSH_BYTES >> 20} MiB write then {FLUSH_BYTES >> 20} MiB read, "
+              "untimed)",
     }
 
 
@@ -262,6 +281,7 @@ def run_gb300(args):
     import torch
 
     from reduction_rdx_sum_gb300 import abi
+    from reduction_rdx_sum_gb300.runop import L2Flush
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -288,12 +308,12 @@ def run_gb300(args):
             out = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=dev)
             fn = abi.SCALAR_OPS[w.op]
         ops.append((w, fn, x, out))
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, FLUSH_BYTES)
     stream = torch.cuda.current_stream(dev)
 
     def one_step(record):
         for k, (w, fn, x, out) in enumerate(ops):
-            flush.zero_()
+            flush()
             if record is not None:
                 record[k][0].record(stream)
             fn(x, out=out, stream=stream)
@@ -333,8 +353,7 @@ def run_gb300(args):
     wtop = ops[top][0]
     achieved = wtop.bytes_read / (float(launch_ms[:, top].mean()) * 1e-3) / 1e9
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(wtop.name)
-    traffic = traffic["bytes_per_launch"] if traffic and traffic.get("source_hash") == src_hash else None
+    traffic = ncu_traffic(wtop.name)
 
     # ---- ladder (the page's five block reductions) on the fp32 array --------
     ladder = {}
@@ -343,7 +362,7 @@ def run_gb300(args):
         part = torch.empty(abi.rdx_ladder_num_partials(v, x2.numel()), dtype=torch.float32, device=dev)
         ts = []
         for it in range(max(3, min(args.steps, 10)) + 2):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             abi.rdx_ladder_partials_f32(v, x2, out=part, stream=stream)

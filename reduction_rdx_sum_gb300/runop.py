@@ -1,0 +1,91 @@
+"""Run one reduction entry point on a seeded synthetic input and time it.
+
+For quick timings and for profilers (one kernel, a few launches, a chosen size):
+
+    python -m reduction_rdx_sum_gb300.runop --op sum_bf16 --n 268435456 --iters 3
+    python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 262144 --cols 256
+
+Before each timed call the L2 is flushed (a write of 512 MiB, then a read of
+512 MiB so that no dirty line is left for the timed kernel to write back).
+Prints one JSON line per call: microseconds (CUDA events on the launching
+stream) and GB/s of input read.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+import torch
+
+from . import abi, inputs
+
+OPS = ("sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32", "rowsum_f32", "sum_f32_noalloc")
+
+
+def make_input(op: str, n: int, rows: int, cols: int, seed: int, dev) -> torch.Tensor:
+    if op in ("sum_bf16", "sumsq_bf16"):
+        return torch.from_numpy(inputs.normal_bf16_bits(n, seed).view(np.int16)).to(dev)
+    if op == "sum_i32":
+        return torch.from_numpy(inputs.integers_i32(n, seed, -(1 << 20), 1 << 20)).to(dev)
+    if op == "rowsum_f32":
+        return torch.from_numpy(inputs.uniform_f32(rows * cols, seed, -1.0, 1.0).reshape(rows, cols)).to(dev)
+    return torch.from_numpy(inputs.normal_f32(n, seed)).to(dev)
+
+
+def entry(op: str):
+    if op == "rowsum_f32":
+        return abi.rdx_rowsum_f32
+    if op == "sum_f32_noalloc":
+        return abi.rdx_sum_f32_noalloc
+    return abi.SCALAR_OPS[op]
+
+
+class L2Flush:
+    """Evict the L2 without leaving dirty lines: write a buffer larger than the
+    L2, then read another one (the read evicts the written lines, paying their
+    write-back outside the timed region)."""
+
+    def __init__(self, dev, nbytes: int = 512 << 20):
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        return self.r.sum()
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--op", choices=OPS, required=True)
+    ap.add_argument("--n", type=int, default=1 << 28)
+    ap.add_argument("--rows", type=int, default=8192)
+    ap.add_argument("--cols", type=int, default=32768)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-flush", action="store_true")
+    args = ap.parse_args(argv)
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
+    fn = entry(args.op)
+    stream = torch.cuda.current_stream(dev)
+    flush = None if args.no_flush else L2Flush(dev)
+    nbytes = x.numel() * x.element_size()
+    for i in range(args.iters):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        out = fn(x, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3
+        print(json.dumps({"op": args.op, "iter": i, "us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
+                          "bytes": nbytes, "result": out.flatten()[0].item()}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

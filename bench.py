@@ -51,10 +51,24 @@ FLUSH_BYTES = 512 << 20
 # and their hash at capture time: a figure is reported only while those files
 # are unchanged.  The captures ran on n = 2^28 and are scaled to the full launch
 # by the element count (traffic grows in proportion).
+_RED = ("device.cuh", "reduce.cu")
+_ROW = ("device.cuh", "rowsum.cu")
+_RED_HASH = "147a71536f24f2ee"
+_ROW_HASH = "f979f18195534618"
 NCU_TRAFFIC = {
-    "c5_sum_bf16": {"bytes_per_launch": 2160926734, "sources": ("device.cuh", "reduce.cu"),
-                    "source_hash": "ff7c06a006ddd0e2",
+    # workload: bytes per full launch, scaled from the capture named in the profile
+    "c5_sum_bf16": {"bytes_per_launch": 2159688718, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
+    "c5_sumsq_bf16": {"bytes_per_launch": 2158935054, "sources": _RED, "source_hash": _RED_HASH,
+                      "profile": "profiles/kernels_dram_traffic_small_cases.md"},
+    "c3_sum_i32": {"bytes_per_launch": 1079446528, "sources": _RED, "source_hash": _RED_HASH,
+                   "profile": "profiles/kernels_dram_traffic_small_cases.md"},
+    "c2_sum_f32": {"bytes_per_launch": 67489172, "sources": _RED, "source_hash": _RED_HASH,
+                   "profile": "profiles/kernels_dram_traffic_small_cases.md"},
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1085277184, "sources": _ROW, "source_hash": _ROW_HASH,
+                             "profile": "profiles/kernels_dram_traffic_small_cases.md"},
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086365696, "sources": _ROW, "source_hash": _ROW_HASH,
+                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 
 
@@ -347,7 +361,8 @@ def run_gb300(args):
         med = float(np.median(launch_ms[:, k]))
         gbs = w.bytes_read / (med * 1e-3) / 1e9
         per_config[w.name] = {"us": round(med * 1e3, 2), "GB/s": round(gbs, 1),
-                              "frac_of_peak": round(gbs / peak, 4), "bytes": w.bytes_read}
+                              "frac_of_peak": round(gbs / peak, 4), "bytes": w.bytes_read,
+                              "ncu_traffic": ncu_traffic(w.name)}
     shares = launch_ms.sum(axis=0) / launch_ms.sum()
     top = int(np.argmax(shares))
     wtop = ops[top][0]

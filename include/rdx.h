@@ -105,6 +105,22 @@ rdx_status rdx_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaS
 rdx_status rdx_sum_i32_i64(const int32_t* x, int64_t n, int64_t* out, cudaStream_t stream);
 
 /*
+ * rdx_sum_sumsq_f32: out2[0] = sum_{i<n} x[i], out2[1] = sum_{i<n} x[i]^2,
+ * both in one pass over x (the input is read once for both results).  Each
+ * component follows the summation tree of rdx_sum_f32 / rdx_sumsq_f32; the
+ * grid may differ from theirs, so the bits may too (within the same bounds).
+ *   out2  two float32 values, 8-byte aligned
+ * Other arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_sum_sumsq_f32(const float* x, int64_t n, float* out2, cudaStream_t stream);
+
+/*
+ * rdx_sum_sumsq_bf16_f32acc: out2[0] = sum, out2[1] = sum of squares of a
+ * bfloat16 array in one pass, float32 accumulation.  out2 as above.
+ */
+rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, cudaStream_t stream);
+
+/*
  * rdx_rowsum_f32: out[r] = sum_{j<cols} x[r*cols + j] for r < rows.
  * The row-segmented sum: on the page each block of versions 1-3 writes the
  * sum of B consecutive inputs (2B for versions 4-5) to out[blockIdx], i.e. a
@@ -156,10 +172,10 @@ int64_t rdx_ladder_num_partials(int version, int64_t n);
  *
  * Same kernel, grid and summation order as rdx_sum_f32, so the same result.
  * Scratch (block partials and a completion counter) lives in one static
- * device array of 16 KiB + 256 B that every GPU loading this library holds
- * until the process exits.  Limit: 4096 block partials; a launch that would
- * need more (a device with more SMs than this library was sized for) is
- * refused with RDX_ERR_INVALID_ARG and a message in rdx_last_cuda_error().
+ * device array of 32 KiB + 256 B that every GPU loading this library holds
+ * until the process exits.  Limit: 8192 block partials, the most any call
+ * of this library's tiling uses; a launch that would need more is refused
+ * with RDX_ERR_INVALID_ARG and a message in rdx_last_cuda_error().
  * All calls share the array and it keeps the last call's contents; the
  * counter is cleared on `stream` before every launch.  Calls whose kernels
  * overlap on the GPU (unordered streams) race on the array: order them.

@@ -56,7 +56,7 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         for name in ("rdx_sum_f32", "rdx_sumsq_f32", "rdx_sum_bf16_f32acc", "rdx_sumsq_bf16_f32acc",
-                     "rdx_sum_i32_i64"):
+                     "rdx_sum_i32_i64", "rdx_sum_sumsq_f32", "rdx_sum_sumsq_bf16_f32acc"):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [vp, i64, vp, vp], i32
         lib.rdx_rowsum_f32.argtypes, lib.rdx_rowsum_f32.restype = [vp, i64, i64, vp, vp], i32
@@ -103,10 +103,10 @@ def _output(out, like: torch.Tensor, dtype, shape) -> torch.Tensor:
     return out
 
 
-def _scalar(name: str, x: torch.Tensor, dtypes, out_dtype, out, stream) -> torch.Tensor:
+def _scalar(name: str, x: torch.Tensor, dtypes, out_dtype, out, stream, shape=()) -> torch.Tensor:
     lib = load()
     x = _input(x, dtypes, name)
-    out = _output(out, x, out_dtype, ())
+    out = _output(out, x, out_dtype, shape)
     with torch.cuda.device(x.device):
         st = getattr(lib, name)(x.data_ptr(), x.numel(), out.data_ptr(), _stream_handle(stream, x.device))
     _check(name, st)
@@ -139,6 +139,16 @@ def rdx_sumsq_bf16_f32acc(x: torch.Tensor, out: torch.Tensor | None = None, stre
 def rdx_sum_i32_i64(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """0-d int64 tensor: the exact sum of an int32 tensor."""
     return _scalar("rdx_sum_i32_i64", x, (torch.int32,), torch.int64, out, stream)
+
+
+def rdx_sum_sumsq_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """(2,) float32 tensor [sum, sum of squares] of a float32 tensor, one pass."""
+    return _scalar("rdx_sum_sumsq_f32", x, (torch.float32,), torch.float32, out, stream, shape=(2,))
+
+
+def rdx_sum_sumsq_bf16_f32acc(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """(2,) float32 tensor [sum, sum of squares] of a bfloat16 tensor, one pass."""
+    return _scalar("rdx_sum_sumsq_bf16_f32acc", x, _BF16, torch.float32, out, stream, shape=(2,))
 
 
 def rdx_rowsum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -196,4 +206,10 @@ SCALAR_OPS = {
     "sum_bf16": rdx_sum_bf16_f32acc,
     "sumsq_bf16": rdx_sumsq_bf16_f32acc,
     "sum_i32": rdx_sum_i32_i64,
+}
+
+# One-pass [sum, sum of squares] entry points by input type.
+PAIR_OPS = {
+    "f32": rdx_sum_sumsq_f32,
+    "bf16": rdx_sum_sumsq_bf16_f32acc,
 }

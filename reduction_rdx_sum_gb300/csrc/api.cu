@@ -28,11 +28,10 @@ std::mutex g_mu;
 std::map<int, DeviceCaps> g_caps;                          // by device ordinal
 std::map<std::pair<int, uintptr_t>, void*> g_workspaces;  // by (device, stream)
 
-// Workspace layout: [completion counter, padded to 256 B][block partials].
+// Workspace layout: [completion counter, padded to 256 B][tile partials].
 constexpr size_t kCounterBytes = 256;
-constexpr int kMaxBlocksPerSm = 32;  // hardware limit of resident blocks per SM
 
-size_t workspace_bytes(const DeviceCaps& c) { return kCounterBytes + size_t(c.sms) * kMaxBlocksPerSm * 8; }
+size_t workspace_bytes() { return kCounterBytes + size_t(rdx::reduce_max_partials()) * 8; }
 
 bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
@@ -60,15 +59,7 @@ rdx_status current_device(const DeviceCaps** out) {
                            "." + std::to_string(c.cc_minor) + "; this library is built for sm_103a only";
             return RDX_ERR_UNSUPPORTED_DEVICE;
         }
-        for (int op = 0; op < int(Op::kCount); ++op) {
-            if ((e = rdx::reduce_blocks_per_sm(Op(op), &c.reduce_bps[op])) != cudaSuccess)
-                return fail_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e);
-            if (c.reduce_bps[op] < 1 || c.reduce_bps[op] > kMaxBlocksPerSm) {
-                t_last_error = "unexpected occupancy for a reduce kernel";
-                return RDX_ERR_CUDA;
-            }
-        }
-        if ((e = rdx::rowsum_blocks_per_sm(&c.rowsum_cta_bps, &c.rowsum_warp_bps)) != cudaSuccess)
+        if ((e = rdx::rowsum_blocks_per_sm(&c.rowsum_cta_bps, &c.rowsum_group_bps)) != cudaSuccess)
             return fail_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e);
         it = g_caps.emplace(dev, c).first;
     }
@@ -92,7 +83,7 @@ rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** o
         return RDX_ERR_ALLOC;
     }
     void* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, workspace_bytes(dev));
+    cudaError_t e = cudaMalloc(&p, workspace_bytes());
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         t_last_error = std::string("cudaMalloc of the workspace: ") + cudaGetErrorString(e);
@@ -120,17 +111,16 @@ rdx_status reduce_entry(Op op, const void* x, int64_t n, void* out, cudaStream_t
     rdx_status st = current_device(&dev);
     if (st != RDX_OK) return st;
 
-    const int64_t head = rdx::reduce_head(op, x, n);
-    const int grid = rdx::reduce_grid(*dev, op, n, head);
+    const rdx::ReducePlan plan = rdx::reduce_plan(op, x, n);
     unsigned* counter = nullptr;
     void* partials = nullptr;
-    if (grid > 1) {
+    if (plan.grid > 1) {
         void* ws = nullptr;
         if ((st = stream_workspace(*dev, stream, &ws)) != RDX_OK) return st;
         counter = static_cast<unsigned*>(ws);
         partials = static_cast<char*>(ws) + kCounterBytes;
     }
-    const cudaError_t e = rdx::reduce_launch(op, x, n, head, partials, counter, out, grid, stream);
+    const cudaError_t e = rdx::reduce_launch(op, x, n, plan, partials, counter, out, stream);
     if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
     return RDX_OK;
 }
@@ -159,6 +149,14 @@ rdx_status rdx_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaS
 
 rdx_status rdx_sum_i32_i64(const int32_t* x, int64_t n, int64_t* out, cudaStream_t stream) {
     return reduce_entry(Op::SumI32, x, n, out, stream);
+}
+
+rdx_status rdx_sum_sumsq_f32(const float* x, int64_t n, float* out2, cudaStream_t stream) {
+    return reduce_entry(Op::SumSumSqF32, x, n, out2, stream);
+}
+
+rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, cudaStream_t stream) {
+    return reduce_entry(Op::SumSumSqBF16, x, n, out2, stream);
 }
 
 rdx_status rdx_rowsum_f32(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {

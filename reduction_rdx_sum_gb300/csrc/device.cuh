@@ -37,8 +37,19 @@ __device__ __forceinline__ void batch_fence(uint4 (&v)[N]) {
 // Term policies.  Each describes one reduction: the input element type, the
 // accumulator, how one element becomes a term, and how the 16-byte vector of
 // V elements becomes one accumulator value (a fixed pairwise tree, so every
-// run adds the same operands in the same order).
+// run adds the same operands in the same order).  Float policies keep one
+// accumulator per load in flight (shorter rounding chains); exact ones may
+// declare kExact and share one.
 // ---------------------------------------------------------------------------
+
+template <class P, class = void>
+struct is_exact {
+    static constexpr bool value = false;
+};
+template <class P>
+struct is_exact<P, decltype(void(P::kExact))> {
+    static constexpr bool value = P::kExact;
+};
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -93,11 +104,65 @@ struct SumI32 {
     using In = int32_t;
     using Acc = long long;
     static constexpr int kVec = 4;
+    // int64 addition is exact and associative: the grouping cannot change the
+    // result, so one accumulator per thread is enough (and saves registers).
+    static constexpr bool kExact = true;
     __device__ static Acc term(In v) { return Acc(v); }
     __device__ static Acc fold(uint4 v) {
         return (Acc(int32_t(v.x)) + Acc(int32_t(v.y))) + (Acc(int32_t(v.z)) + Acc(int32_t(v.w)));
     }
 };
+
+// Sum and sum of squares carried together (one pass over the input for both).
+// Each component is added in exactly the order the single reductions use.
+struct __align__(8) SumSq2 {
+    float s;  // sum
+    float q;  // sum of squares
+    SumSq2() = default;
+    __host__ __device__ explicit SumSq2(float v) : s(v), q(v) {}
+    __host__ __device__ SumSq2(float s_, float q_) : s(s_), q(q_) {}
+};
+__device__ __forceinline__ SumSq2 operator+(SumSq2 a, SumSq2 b) { return SumSq2(a.s + b.s, a.q + b.q); }
+__device__ __forceinline__ SumSq2& operator+=(SumSq2& a, SumSq2 b) {
+    a.s += b.s;
+    a.q += b.q;
+    return a;
+}
+
+struct SumSumSqF32 {
+    using In = float;
+    using Acc = SumSq2;
+    static constexpr int kVec = 4;
+    __device__ static Acc term(In v) { return Acc(SumF32::term(v), SumSqF32::term(v)); }
+    __device__ static Acc fold(uint4 v) { return Acc(SumF32::fold(v), SumSqF32::fold(v)); }
+};
+
+struct SumSumSqBF16 {
+    using In = uint16_t;
+    using Acc = SumSq2;
+    static constexpr int kVec = 8;
+    __device__ static Acc term(In v) { return Acc(SumBF16::term(v), SumSqBF16::term(v)); }
+    __device__ static Acc fold(uint4 v) { return Acc(SumBF16::fold(v), SumSqBF16::fold(v)); }
+};
+
+// ---------------------------------------------------------------------------
+// Shuffle and coherent-load overloads for the accumulator types.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float shfl_down(float v, int off) { return __shfl_down_sync(kFullMask, v, off); }
+__device__ __forceinline__ long long shfl_down(long long v, int off) { return __shfl_down_sync(kFullMask, v, off); }
+__device__ __forceinline__ SumSq2 shfl_down(SumSq2 v, int off) {
+    return SumSq2(shfl_down(v.s, off), shfl_down(v.q, off));
+}
+
+// Loads of values other blocks wrote in this kernel: through L2 (ld.global.cg),
+// never a stale L1 line.
+__device__ __forceinline__ float load_cg(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ long long load_cg(const long long* p) { return __ldcg(p); }
+__device__ __forceinline__ SumSq2 load_cg(const SumSq2* p) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+    return SumSq2(v.x, v.y);
+}
 
 // ---------------------------------------------------------------------------
 // Trees.
@@ -109,7 +174,7 @@ struct SumI32 {
 template <class T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll
-    for (int off = kWarpSize / 2; off > 0; off >>= 1) v += __shfl_down_sync(kFullMask, v, off);
+    for (int off = kWarpSize / 2; off > 0; off >>= 1) v += shfl_down(v, off);
     return v;
 }
 

@@ -8,39 +8,43 @@
 
 namespace rdx {
 
-// The scalar reductions of the C ABI.
-enum class Op : int { SumF32 = 0, SumSqF32, SumBF16, SumSqBF16, SumI32, kCount };
+// The scalar reductions of the C ABI (the last two give sum and sum of squares
+// in one pass).
+enum class Op : int { SumF32 = 0, SumSqF32, SumBF16, SumSqBF16, SumI32, SumSumSqF32, SumSumSqBF16, kCount };
 
 // Properties of the current device that the launch heuristics need.
 struct DeviceCaps {
     int ordinal = -1;
-    int sms = 0;             // streaming multiprocessors
+    int sms = 0;  // streaming multiprocessors
     int cc_major = 0;
     int cc_minor = 0;
-    int reduce_bps[int(Op::kCount)] = {};  // resident blocks per SM, per reduce kernel
-    int rowsum_cta_bps = 0;
-    int rowsum_warp_bps = 0;
+    int rowsum_cta_bps = 0;    // resident blocks per SM of the long-row kernel
+    int rowsum_group_bps = 0;  // resident blocks per SM of the short-row kernel
 };
 
 // ---- scalar reductions (reduce.cu) ----------------------------------------
+// How one call is cut: `head` elements before the first 16-byte boundary of x,
+// then tiles of `tile` 16-byte vectors, one block each (`grid` blocks, at most
+// reduce_max_partials()).  Depends only on n and x's alignment.
+struct ReducePlan {
+    int64_t head = 0;
+    int64_t tile = 0;
+    int64_t grid = 1;
+};
 int reduce_block_threads();
 int reduce_unroll();
+int64_t reduce_max_partials();
 int reduce_vec_elems(Op op);
 size_t reduce_elem_bytes(Op op);
 size_t reduce_acc_bytes(Op op);
-cudaError_t reduce_blocks_per_sm(Op op, int* blocks);
-// Grid for n elements starting at address x: whole waves of resident blocks,
-// fewer when n is too small to give every thread one unrolled iteration.
-// Depends on n, the alignment of x and the device only.
-int reduce_grid(const DeviceCaps& dev, Op op, int64_t n, int64_t head);
-// head = elements before the first 16-byte boundary of x (at most n).
-int64_t reduce_head(Op op, const void* x, int64_t n);
-// partials: grid accumulator slots; ticket: a zeroed completion counter.
-cudaError_t reduce_launch(Op op, const void* x, int64_t n, int64_t head, void* partials,
-                          unsigned* ticket, void* out, int grid, cudaStream_t stream);
+ReducePlan reduce_plan(Op op, const void* x, int64_t n);
+// partials: plan.grid accumulator slots (reduce_acc_bytes each); counter: a
+// zeroed completion counter.  Neither is touched when plan.grid == 1.
+cudaError_t reduce_launch(Op op, const void* x, int64_t n, const ReducePlan& plan, void* partials,
+                          unsigned* counter, void* out, cudaStream_t stream);
 
 // ---- row-segmented sum (rowsum.cu) ----------------------------------------
-cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* warp_bps);
+cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps);
 cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
                           cudaStream_t stream);
 

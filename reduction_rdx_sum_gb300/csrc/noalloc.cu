@@ -16,15 +16,15 @@
 // fixed-size array in the library's static device memory instead.
 //
 // Scratch: kScratchBytes = 256-byte completion counter + kMaxPartials float32
-// block partials (16 KiB + 256 B).  The array exists on every GPU that loads
+// block partials (32 KiB + 256 B).  The array exists on every GPU that loads
 // the library and stays there until the process exits.  All calls share it:
 // the counter is cleared on the caller's stream before every launch, and two
 // calls whose kernels run at the same time on the GPU (different streams, no
 // ordering between them) race on it and give wrong results.
 //
-// Set-up: the first call on each device, with that device current, looks up
-// the device address of the array (cudaGetSymbolAddress) and the device's SM
-// count and occupancy.  Make that first call before any stream capture.
+// Set-up: the first call on each device, with that device current, checks
+// the device and looks up the device address of the array
+// (cudaGetSymbolAddress).  Make that first call before any stream capture.
 #include "rdx.h"
 
 #include <climits>
@@ -35,7 +35,7 @@
 
 namespace {
 
-constexpr int kMaxPartials = 4096;  // block partials the scratch holds
+constexpr int kMaxPartials = 8192;  // block partials the scratch holds
 constexpr size_t kCounterBytes = 256;
 constexpr size_t kScratchBytes = kCounterBytes + size_t(kMaxPartials) * sizeof(float);
 
@@ -79,9 +79,6 @@ rdx_status setup_current_device(const DeviceSetup** out) {
             return fail_cuda("cudaDeviceGetAttribute", e);
         if (c.cc_major != 10 || c.cc_minor != 3)
             return fail(RDX_ERR_UNSUPPORTED_DEVICE, "this library is built for sm_103a only");
-        const int op = int(rdx::Op::SumF32);
-        if ((e = rdx::reduce_blocks_per_sm(rdx::Op::SumF32, &c.reduce_bps[op])) != cudaSuccess)
-            return fail_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e);
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
             return fail_cuda("cudaGetSymbolAddress of the static scratch", e);
@@ -113,18 +110,17 @@ extern "C" rdx_status rdx_sum_f32_noalloc(const float* x, int64_t n, float* out,
     rdx_status st = setup_current_device(&s);
     if (st != RDX_OK) return st;
 
-    const int64_t head = rdx::reduce_head(rdx::Op::SumF32, x, n);
-    const int grid = rdx::reduce_grid(s->caps, rdx::Op::SumF32, n, head);
-    if (grid > kMaxPartials)
-        return fail(RDX_ERR_INVALID_ARG, "rdx_sum_f32_noalloc: this launch needs " + std::to_string(grid) +
+    const rdx::ReducePlan plan = rdx::reduce_plan(rdx::Op::SumF32, x, n);
+    if (plan.grid > kMaxPartials)
+        return fail(RDX_ERR_INVALID_ARG, "rdx_sum_f32_noalloc: this launch needs " + std::to_string(plan.grid) +
                                              " block partials; the static scratch holds " +
                                              std::to_string(kMaxPartials));
 
     unsigned char* scratch = static_cast<unsigned char*>(s->scratch);
     cudaError_t e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
     if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync of the completion counter", e);
-    e = rdx::reduce_launch(rdx::Op::SumF32, x, n, head, scratch + kCounterBytes,
-                           reinterpret_cast<unsigned*>(scratch), out, grid, stream);
+    e = rdx::reduce_launch(rdx::Op::SumF32, x, n, plan, scratch + kCounterBytes,
+                           reinterpret_cast<unsigned*>(scratch), out, stream);
     if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
     return RDX_OK;
 }

@@ -1,23 +1,27 @@
 // reduce.cu -- one-pass scalar sum reductions (float32, float32 squares,
-// bfloat16 -> float32, int32 -> int64) with a deterministic on-device finish.
+// bfloat16 -> float32, int32 -> int64, and sum + sum of squares together)
+// with a deterministic on-device finish.
 //
 // The page "03_shared_memory_sync_reduction.py", demo 3, walks from a
 // divergent shared-memory tree (version 1) to "first add during load" plus a
 // warp-shuffle finish (version 5), and ends each kernel with one partial per
 // block that the host adds up.  This kernel keeps version 5's shape and takes
-// its two ideas further for a GPU with 152 SMs and HBM3e:
-//   * add on load: each thread walks the array in grid-stride order with
-//     kUnroll independent 16-byte loads in flight and folds each vector into
-//     its own register accumulator (version 4's two elements per thread become
-//     thousands);
+// its ideas further for a GPU with 152 SMs and HBM3e:
+//   * tiles: the 16-byte-aligned body of the input is cut into equal
+//     contiguous tiles, one block per tile (128 KiB tiles for a 1 GiB input,
+//     at most kMaxTiles tiles); the hardware hands tiles to SMs as they free
+//     up, so a slow SM does not hold back the end of the kernel;
+//   * add on load: inside its tile each thread keeps kUnroll independent
+//     16-byte loads in flight and folds each vector into its own register
+//     accumulator (version 4's two elements per thread become dozens);
 //   * shuffle trees: a warp tree, then one shared-memory word per warp, then
-//     a warp tree over those words (the shared-memory tree of versions 1-4 is
-//     gone; one barrier per block);
-//   * the per-block partials are finished on the device: the block that
-//     arrives last at a completion counter (acquire-release atomic) adds all
-//     partials in a fixed order and resets the counter.  Nothing waits on
-//     anything, and no float atomics are used, so the result does not depend
-//     on which block finishes first.
+//     a warp tree over those words (one barrier per block);
+//   * the tile partials are finished on the device: the block that arrives
+//     last at a completion counter (acquire-release atomic) adds all partials
+//     in a fixed order and resets the counter.  Nothing waits on anything,
+//     and no float atomics are used.
+// The tiling depends only on n and the input's 16-byte alignment, so the
+// summation order, and the result, are the same on every run and every GPU.
 #include "device.cuh"
 #include "launch.h"
 
@@ -25,15 +29,28 @@
 #define RDX_REDUCE_BLOCK 256
 #endif
 #ifndef RDX_REDUCE_UNROLL
-#define RDX_REDUCE_UNROLL 8
+#define RDX_REDUCE_UNROLL 4
+#endif
+#ifndef RDX_REDUCE_MAX_TILES
+#define RDX_REDUCE_MAX_TILES 8192
+#endif
+#ifndef RDX_REDUCE_MIN_TILE
+#define RDX_REDUCE_MIN_TILE 1024
 #endif
 
 namespace rdx {
 namespace {
 
-constexpr int kBlock = RDX_REDUCE_BLOCK;    // threads per block
-constexpr int kUnroll = RDX_REDUCE_UNROLL;  // 16-byte loads in flight per thread
+constexpr int kBlock = RDX_REDUCE_BLOCK;                  // threads per block
+constexpr int kUnroll = RDX_REDUCE_UNROLL;                // 16-byte loads in flight per thread
+constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // upper bound on blocks (= partials)
+constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per tile, at least
+constexpr int kFinishLoadBytes = 32;                      // partial bytes in flight per thread, last block
+// 8 resident blocks of 256 threads fill an SM (2048 threads): at most 32
+// registers per thread, so every dtype streams with full occupancy.
+constexpr int kMinBlocksPerSm = 2048 / kBlock;
 static_assert((kUnroll & (kUnroll - 1)) == 0, "kUnroll must be a power of two");
+static_assert(kMinTile % kBlock == 0, "tiles are whole multiples of the block");
 
 // Completion counter: acquire-release at GPU scope, so the partial this
 // thread stored before is visible to the block that draws the last ticket,
@@ -48,8 +65,8 @@ __device__ __forceinline__ unsigned take_ticket(unsigned* counter) {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kBlock)
-reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head,
+__global__ void __launch_bounds__(kBlock, kMinBlocksPerSm)
+reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head, int64_t tile,
               typename P::Acc* __restrict__ partials, unsigned* __restrict__ counter,
               typename P::Acc* __restrict__ out) {
     using Acc = typename P::Acc;
@@ -57,34 +74,40 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head,
     __shared__ Acc smem[kBlock / kWarpSize];
     __shared__ unsigned last_block;
 
-    const int64_t nthreads = int64_t(gridDim.x) * kBlock;
-    const int64_t g = int64_t(blockIdx.x) * kBlock + threadIdx.x;
     const int64_t m = (n - head) / V;  // whole 16-byte vectors after the head
-    const int64_t tail0 = head + m * V;
+    const int64_t t0 = int64_t(blockIdx.x) * tile;
+    const int64_t t1 = t0 + tile < m ? t0 + tile : m;
     const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(x + head);
 
+    // accumulator of load slot u: its own for float sums, a shared one for
+    // exact (integer) sums
+    constexpr bool kShared = is_exact<P>::value;
+    auto kAccOf = [](int u) { return kShared ? 0 : u; };
     Acc acc[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) acc[u] = Acc(0);
 
     // Fewer than V elements before the first 16-byte boundary and after the
-    // last whole vector: the first threads take one each.
-    if (g < head) acc[0] += P::term(x[g]);
-    if (g < n - tail0) acc[kUnroll - 1] += P::term(x[tail0 + g]);
+    // last whole vector: the first threads of block 0 take one each.
+    if (blockIdx.x == 0) {
+        const int64_t tail0 = head + m * V;
+        if (threadIdx.x < head) acc[0] += P::term(x[threadIdx.x]);
+        if (threadIdx.x < n - tail0) acc[kUnroll - 1] += P::term(x[tail0 + threadIdx.x]);
+    }
 
-    int64_t i = g;
-    for (; i + (kUnroll - 1) * nthreads < m; i += kUnroll * nthreads) {
+    int64_t i = t0 + threadIdx.x;
+    for (; i + (kUnroll - 1) * kBlock < t1; i += kUnroll * kBlock) {
         uint4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(xv + i + u * nthreads);
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(xv + i + u * kBlock);
         batch_fence(v);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) acc[u] += P::fold(v[u]);
+        for (int u = 0; u < kUnroll; ++u) acc[kAccOf(u)] += P::fold(v[u]);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        const int64_t j = i + u * nthreads;
-        if (j < m) acc[u] += P::fold(ld_stream16(xv + j));
+        const int64_t j = i + u * kBlock;
+        if (j < t1) acc[kAccOf(u)] += P::fold(ld_stream16(xv + j));
     }
 
     Acc a = block_sum<kBlock>(fold_array(acc), smem);
@@ -100,82 +123,87 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head,
     __syncthreads();
     if (!last_block) return;
 
-    // The last block: every partial is in place.  Add them in block order
-    // (thread t takes t, t + kBlock, ...; then the block tree).
-    Acc b = Acc(0);
-    for (int j = threadIdx.x; j < int(gridDim.x); j += kBlock) b += __ldcg(partials + j);
-    b = block_sum<kBlock>(b, smem);
+    // The last block: every partial is in place.  Thread t adds partials
+    // t, t + kBlock, ... (kFinishUnroll independent chains, loads in flight
+    // together), then the block tree.
+    constexpr int kFinishUnroll = kFinishLoadBytes / int(sizeof(Acc));
+    Acc b[kFinishUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinishUnroll; ++u) b[u] = Acc(0);
+    const int g = int(gridDim.x);
+    int j = threadIdx.x;
+    for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
+        Acc p[kFinishUnroll];
+#pragma unroll
+        for (int u = 0; u < kFinishUnroll; ++u) p[u] = load_cg(partials + j + u * kBlock);
+#pragma unroll
+        for (int u = 0; u < kFinishUnroll; ++u) b[u] += p[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kFinishUnroll; ++u) {
+        if (j + u * kBlock < g) b[u] += load_cg(partials + j + u * kBlock);
+    }
+    const Acc total = block_sum<kBlock>(fold_array(b), smem);
     if (threadIdx.x == 0) {
-        *out = b;
+        *out = total;
         *counter = 0u;  // ready for the next call on this stream
     }
 }
 
 template <class P>
-cudaError_t launch_typed(const void* x, int64_t n, int64_t head, void* partials, unsigned* counter, void* out,
-                         int grid, cudaStream_t stream) {
-    reduce_kernel<P><<<grid, kBlock, 0, stream>>>(static_cast<const typename P::In*>(x), n, head,
-                                                   static_cast<typename P::Acc*>(partials), counter,
-                                                   static_cast<typename P::Acc*>(out));
+cudaError_t launch_typed(const void* x, int64_t n, const ReducePlan& plan, void* partials, unsigned* counter,
+                         void* out, cudaStream_t stream) {
+    reduce_kernel<P><<<unsigned(plan.grid), kBlock, 0, stream>>>(
+        static_cast<const typename P::In*>(x), n, plan.head, plan.tile, static_cast<typename P::Acc*>(partials),
+        counter, static_cast<typename P::Acc*>(out));
     return cudaGetLastError();
-}
-
-template <class P>
-cudaError_t occupancy_typed(int* blocks) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, reduce_kernel<P>, kBlock, 0);
 }
 
 }  // namespace
 
 int reduce_block_threads() { return kBlock; }
 int reduce_unroll() { return kUnroll; }
+int64_t reduce_max_partials() { return kMaxTiles; }
 
 int reduce_vec_elems(Op op) {
     switch (op) {
         case Op::SumBF16:
-        case Op::SumSqBF16: return 8;
+        case Op::SumSqBF16:
+        case Op::SumSumSqBF16: return 8;
         default: return 4;
     }
 }
 
 size_t reduce_elem_bytes(Op op) { return 16 / size_t(reduce_vec_elems(op)); }
 
-size_t reduce_acc_bytes(Op op) { return op == Op::SumI32 ? 8 : 4; }
-
-cudaError_t reduce_blocks_per_sm(Op op, int* blocks) {
-    switch (op) {
-        case Op::SumF32: return occupancy_typed<SumF32>(blocks);
-        case Op::SumSqF32: return occupancy_typed<SumSqF32>(blocks);
-        case Op::SumBF16: return occupancy_typed<SumBF16>(blocks);
-        case Op::SumSqBF16: return occupancy_typed<SumSqBF16>(blocks);
-        case Op::SumI32: return occupancy_typed<SumI32>(blocks);
-        default: return cudaErrorInvalidValue;
-    }
+size_t reduce_acc_bytes(Op op) {
+    return (op == Op::SumI32 || op == Op::SumSumSqF32 || op == Op::SumSumSqBF16) ? 8 : 4;
 }
 
-int64_t reduce_head(Op op, const void* x, int64_t n) {
+ReducePlan reduce_plan(Op op, const void* x, int64_t n) {
+    ReducePlan p;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(x) & 15u;
-    const int64_t head = mis ? int64_t((16u - mis) / reduce_elem_bytes(op)) : 0;
-    return head < n ? head : n;
+    p.head = mis ? int64_t((16u - mis) / reduce_elem_bytes(op)) : 0;
+    if (p.head > n) p.head = n;
+    const int64_t m = (n - p.head) / reduce_vec_elems(op);
+    int64_t tile = (m + kMaxTiles - 1) / kMaxTiles;
+    tile = (tile + kBlock - 1) / kBlock * kBlock;  // whole blocks of vectors
+    if (tile < kMinTile) tile = kMinTile;
+    p.tile = tile;
+    p.grid = m > 0 ? (m + tile - 1) / tile : 1;  // <= kMaxTiles
+    return p;
 }
 
-int reduce_grid(const DeviceCaps& dev, Op op, int64_t n, int64_t head) {
-    const int64_t m = (n - head) / reduce_vec_elems(op);
-    const int64_t per_block = int64_t(kBlock) * kUnroll;  // vectors one block loads per iteration
-    const int64_t want = (m + per_block - 1) / per_block;
-    const int64_t cap = int64_t(dev.sms) * dev.reduce_bps[int(op)];
-    int64_t g = want < cap ? want : cap;
-    return int(g < 1 ? 1 : g);
-}
-
-cudaError_t reduce_launch(Op op, const void* x, int64_t n, int64_t head, void* partials, unsigned* counter,
-                          void* out, int grid, cudaStream_t stream) {
+cudaError_t reduce_launch(Op op, const void* x, int64_t n, const ReducePlan& plan, void* partials,
+                          unsigned* counter, void* out, cudaStream_t stream) {
     switch (op) {
-        case Op::SumF32: return launch_typed<SumF32>(x, n, head, partials, counter, out, grid, stream);
-        case Op::SumSqF32: return launch_typed<SumSqF32>(x, n, head, partials, counter, out, grid, stream);
-        case Op::SumBF16: return launch_typed<SumBF16>(x, n, head, partials, counter, out, grid, stream);
-        case Op::SumSqBF16: return launch_typed<SumSqBF16>(x, n, head, partials, counter, out, grid, stream);
-        case Op::SumI32: return launch_typed<SumI32>(x, n, head, partials, counter, out, grid, stream);
+        case Op::SumF32: return launch_typed<SumF32>(x, n, plan, partials, counter, out, stream);
+        case Op::SumSqF32: return launch_typed<SumSqF32>(x, n, plan, partials, counter, out, stream);
+        case Op::SumBF16: return launch_typed<SumBF16>(x, n, plan, partials, counter, out, stream);
+        case Op::SumSqBF16: return launch_typed<SumSqBF16>(x, n, plan, partials, counter, out, stream);
+        case Op::SumI32: return launch_typed<SumI32>(x, n, plan, partials, counter, out, stream);
+        case Op::SumSumSqF32: return launch_typed<SumSumSqF32>(x, n, plan, partials, counter, out, stream);
+        case Op::SumSumSqBF16: return launch_typed<SumSumSqBF16>(x, n, plan, partials, counter, out, stream);
         default: return cudaErrorInvalidValue;
     }
 }

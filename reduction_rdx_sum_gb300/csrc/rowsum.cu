@@ -4,10 +4,12 @@
 // On the page "03_shared_memory_sync_reduction.py", demo 3, every block writes
 // the sum of its own contiguous segment to out[blockIdx]: a segmented sum.
 // Here a segment is a row, and the work per row decides who sums it:
-//   * short rows (cols <= kWarpRowMaxCols): a group of LPR lanes per row
-//     (LPR = 1 .. 32, about four 16-byte vectors per lane), 32/LPR rows per
-//     warp step; a warp finishes 32 consecutive rows and writes their sums as
-//     one coalesced 128-byte store;
+//   * short rows (cols <= kFitRowMaxCols): a group of LPR lanes per row, each
+//     lane holding at most four 16-byte vectors of the row, so a warp sums
+//     32/LPR consecutive rows per step; the loads of kRowSteps steps are
+//     issued together before any of them is reduced;
+//   * medium rows (cols <= kGroupRowMaxCols): a warp per row, looping over
+//     the row four vectors per lane at a time;
 //   * long rows: one block per row, the same add-on-load loop and block tree
 //     as the scalar reduction, a direct store of the row's sum.
 // A row's summation order depends only on its address and length, never on
@@ -18,10 +20,15 @@
 namespace rdx {
 namespace {
 
-constexpr int kCtaBlock = 256;          // threads per row, long rows
-constexpr int kCtaUnroll = 4;           // 16-byte loads in flight per thread, long rows
-constexpr int kWarpBlock = 256;         // threads per block, short rows
-constexpr int64_t kWarpRowMaxCols = 1024;
+constexpr int kCtaBlock = 256;   // threads per row, long rows
+constexpr int kCtaUnroll = 4;    // 16-byte loads in flight per thread, long rows
+constexpr int kGroupBlock = 256; // threads per block, short rows
+constexpr int64_t kGroupRowMaxCols = 4096;
+constexpr int64_t kFitRowMaxCols = 512;  // 4 vectors x 32 lanes x 4 floats
+#ifndef RDX_ROW_STEPS
+#define RDX_ROW_STEPS 1
+#endif
+constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight together
 
 // Elements of a row before its first 16-byte boundary (rows of a matrix with
 // cols % 4 != 0 start at varying alignments).
@@ -58,32 +65,77 @@ __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_
     return fold_array(acc);
 }
 
-// Short rows.  Warp w takes batches of 32 consecutive rows; within a batch,
-// step s has group g (lanes g*LPR .. g*LPR+LPR-1) sum row s*NG + g, and lane
-// i keeps the total of row i, so the 32 sums leave in one coalesced store.
+// Short rows.  Group g of warp w (lanes g*LPR .. g*LPR+LPR-1) sums row
+// (w + k * nwarps) * NG + g for k = 0, 1, ...; lane 0 of the group stores it.
+// The NG rows of one warp step are consecutive, so are their sums.
 template <int LPR>
-__global__ void __launch_bounds__(kWarpBlock)
-rowsum_warp_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
+__global__ void __launch_bounds__(kGroupBlock)
+rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
     constexpr int NG = kWarpSize / LPR;  // rows in flight per warp step
     const int lane = threadIdx.x % kWarpSize;
     const int grp = lane / LPR;
     const int l = lane % LPR;
-    const int64_t warp = (int64_t(blockIdx.x) * kWarpBlock + threadIdx.x) / kWarpSize;
-    const int64_t nwarps = int64_t(gridDim.x) * (kWarpBlock / kWarpSize);
-    const int64_t nbatch = (rows + kWarpSize - 1) / kWarpSize;
-    for (int64_t b = warp; b < nbatch; b += nwarps) {
-        const int64_t r0 = b * kWarpSize;
-        float mine = 0.f;
+    const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
+    const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
+    const int64_t nsteps = (rows + NG - 1) / NG;
+    for (int64_t k = warp; k < nsteps; k += nwarps) {
+        const int64_t r = k * NG + grp;
+        float s = 0.f;
+        if (r < rows) s = row_share<LPR>(x + r * cols, cols, l);
+        s = group_allreduce<LPR>(s);  // every lane takes part, in range or not
+        if (l == 0 && r < rows) out[r] = s;
+    }
+}
+
+// Short rows: every row has at most 4*LPR whole vectors, so one load round
+// covers it.  A warp takes units of kRowSteps*NG consecutive rows; in a unit,
+// step q has group g sum row q*NG + g.  All loads of the unit are issued
+// before the first reduction.  Lane 0 of each group stores its row's sum.
+template <int LPR>
+__global__ void __launch_bounds__(kGroupBlock)
+rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
+    constexpr int NG = kWarpSize / LPR;
+    constexpr int RU = NG * kRowSteps;  // rows per unit
+    const int lane = threadIdx.x % kWarpSize;
+    const int grp = lane / LPR;
+    const int l = lane % LPR;
+    const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
+    const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
+    const int64_t nunits = (rows + RU - 1) / RU;
+    for (int64_t k = warp; k < nunits; k += nwarps) {
+        uint4 v[kRowSteps * 4];
+        float sc[kRowSteps];
 #pragma unroll
-        for (int step = 0; step < LPR; ++step) {
-            const int64_t r = r0 + step * NG + grp;
-            float s = 0.f;
-            if (r < rows) s = row_share<LPR>(x + r * cols, cols, l);
-            s = group_allreduce<LPR>(s);
-            const float t = __shfl_sync(kFullMask, s, (lane % NG) * LPR);
-            if (lane / NG == step) mine = t;
+        for (int q = 0; q < kRowSteps; ++q) {
+            const int64_t r = k * RU + q * NG + grp;
+            sc[q] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[q * 4 + u] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) {
+                const float* __restrict__ row = x + r * cols;
+                const int64_t head = row_head(row, cols);
+                const int64_t m = (cols - head) >> 2;
+                const int64_t tail0 = head + 4 * m;
+                for (int64_t e = l; e < head; e += LPR) sc[q] += __ldg(row + e);
+                for (int64_t e = tail0 + l; e < cols; e += LPR) sc[q] += __ldg(row + e);
+                const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (l + u * LPR < m) v[q * 4 + u] = ld_stream16(rv + l + u * LPR);
+                }
+            }
         }
-        if (r0 + lane < rows) out[r0 + lane] = mine;
+        batch_fence(v);
+#pragma unroll
+        for (int q = 0; q < kRowSteps; ++q) {
+            float acc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] = SumF32::fold(v[q * 4 + u]);
+            acc[0] += sc[q];
+            float s = group_allreduce<LPR>(fold_array(acc));
+            const int64_t r = k * RU + q * NG + grp;
+            if (l == 0 && r < rows) out[r] = s;
+        }
     }
 }
 
@@ -122,46 +174,65 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float
     }
 }
 
-// Lanes per row: about four 16-byte vectors per lane, a power of two <= 32.
+// Lanes per row: the fewest (a power of two, at most 32) that leave each lane
+// at most four 16-byte vectors of the row.
 int lanes_per_row(int64_t cols) {
     const int64_t vecs = cols / 4;
     int lpr = 1;
-    while (lpr < 32 && int64_t(lpr) * 2 * 4 <= vecs) lpr *= 2;
+    while (lpr < 32 && int64_t(lpr) * 4 < vecs) lpr *= 2;
     return lpr;
 }
 
 template <int LPR>
-cudaError_t launch_warp(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
-    constexpr int64_t kWarpsPerBlock = kWarpBlock / kWarpSize;
-    const int64_t nbatch = (rows + kWarpSize - 1) / kWarpSize;
-    int64_t blocks = (nbatch + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks > 0x7fffffff) blocks = 0x7fffffff;
-    rowsum_warp_kernel<LPR><<<unsigned(blocks), kWarpBlock, 0, stream>>>(x, rows, cols, out);
+cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+                       cudaStream_t stream) {
+    constexpr int64_t kRU = (kWarpSize / LPR) * kRowSteps;
+    constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
+    const int64_t nunits = (rows + kRU - 1) / kRU;
+    int64_t blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    // four waves of resident blocks; each warp then loops over its units
+    const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
+    if (blocks > cap) blocks = cap;
+    rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, out);
+    return cudaGetLastError();
+}
+
+template <int LPR>
+cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+                         cudaStream_t stream) {
+    constexpr int64_t kNG = kWarpSize / LPR;
+    constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
+    const int64_t nsteps = (rows + kNG - 1) / kNG;
+    int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    // four waves of resident blocks; each warp then loops over its steps
+    const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
+    if (blocks > cap) blocks = cap;
+    rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, out);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* warp_bps) {
+cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cta_bps, rowsum_cta_kernel, kCtaBlock, 0);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(warp_bps, rowsum_warp_kernel<16>, kWarpBlock, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(group_bps, rowsum_fit_kernel<16>, kGroupBlock, 0);
 }
 
 cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
                           cudaStream_t stream) {
-    (void)dev;
     if (rows <= 0) return cudaSuccess;
-    if (cols <= kWarpRowMaxCols) {
+    if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {
-            case 1: return launch_warp<1>(x, rows, cols, out, stream);
-            case 2: return launch_warp<2>(x, rows, cols, out, stream);
-            case 4: return launch_warp<4>(x, rows, cols, out, stream);
-            case 8: return launch_warp<8>(x, rows, cols, out, stream);
-            case 16: return launch_warp<16>(x, rows, cols, out, stream);
-            default: return launch_warp<32>(x, rows, cols, out, stream);
+            case 1: return launch_fit<1>(dev, x, rows, cols, out, stream);
+            case 2: return launch_fit<2>(dev, x, rows, cols, out, stream);
+            case 4: return launch_fit<4>(dev, x, rows, cols, out, stream);
+            case 8: return launch_fit<8>(dev, x, rows, cols, out, stream);
+            case 16: return launch_fit<16>(dev, x, rows, cols, out, stream);
+            default: return launch_fit<32>(dev, x, rows, cols, out, stream);
         }
     }
+    if (cols <= kGroupRowMaxCols) return launch_group<32>(dev, x, rows, cols, out, stream);
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
     rowsum_cta_kernel<<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, out);
     return cudaGetLastError();

@@ -136,6 +136,45 @@ def test_nonfinite_propagation():
 
 
 # ---------------------------------------------------------------------------
+# one-pass sum and sum of squares
+# ---------------------------------------------------------------------------
+
+def check_pair(kind, host, got):
+    s_op, q_op = ("sum_f32", "sumsq_f32") if kind == "f32" else ("sum_bf16", "sumsq_bf16")
+    check(s_op, host, got[0])
+    check(q_op, host, got[1])
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+@pytest.mark.parametrize("n", SIZES)
+def test_sum_sumsq_parity(kind, n):
+    host = host_input("sum_f32" if kind == "f32" else "sum_bf16", n, seed=n % 89)
+    got = abi.PAIR_OPS[kind](to_device(host)).tolist()
+    check_pair(kind, host, got)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_sum_sumsq_misaligned_and_deterministic(kind):
+    op = "sum_f32" if kind == "f32" else "sum_bf16"
+    for n in (5, 4097, (1 << 20) + 3):
+        host = host_input(op, n, seed=3)
+        for offset in range(1, VEC[op]):
+            check_pair(kind, host, abi.PAIR_OPS[kind](to_device(host, offset)).tolist())
+    x = to_device(host_input(op, (1 << 24) + 13, seed=1))
+    first = abi.PAIR_OPS[kind](x)
+    for _ in range(5):
+        assert torch.equal(abi.PAIR_OPS[kind](x).view(torch.int32), first.view(torch.int32))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", (inputs.CFG2_SUM_F32, inputs.CFG5_SUM_BF16), ids=lambda w: w.name)
+def test_config_sum_sumsq(w):
+    host = workload(w)
+    kind = "f32" if w.op == "sum_f32" else "bf16"
+    check_pair(kind, host, abi.PAIR_OPS[kind](to_device(host)).tolist())
+
+
+# ---------------------------------------------------------------------------
 # the five workload configurations at full size
 # ---------------------------------------------------------------------------
 

@@ -370,6 +370,41 @@ def run_gb300(args):
     src_hash = kernel_source_hash()
     traffic = ncu_traffic(wtop.name)
 
+    # ---- extras: entry points outside the step, timed the same way -----------
+    def time_launches(fn, iters):
+        ts = []
+        for it in range(iters + 2):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    extras = {}
+    iters = max(3, min(args.steps, 10))
+    key2 = (inputs.CFG2_SUM_F32.dist, inputs.CFG2_SUM_F32.seed, inputs.CFG2_SUM_F32.numel)
+    key5 = (inputs.CFG5_SUM_BF16.dist, inputs.CFG5_SUM_BF16.seed, inputs.CFG5_SUM_BF16.numel)
+    pair = torch.empty(2, dtype=torch.float32, device=dev)
+    for name, key, fn in (("c2_sum_sumsq_f32_one_pass", key2, abi.rdx_sum_sumsq_f32),
+                          ("c5_sum_sumsq_bf16_one_pass", key5, abi.rdx_sum_sumsq_bf16_f32acc)):
+        xk = dev_arrays[key]
+        ms = time_launches(lambda: fn(xk, out=pair, stream=stream), iters)
+        nb = xk.numel() * xk.element_size()
+        extras[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1), "bytes": nb,
+                        "replaces_us": round(per_config[name[:2] + ("_sum_f32" if "f32" in name else "_sum_bf16")]["us"]
+                                             + per_config[name[:2] + ("_sumsq_f32" if "f32" in name else "_sumsq_bf16")]
+                                             ["us"], 2)}
+    key4 = (inputs.CFG4_ROWSUM_WIDE.dist, inputs.CFG4_ROWSUM_WIDE.seed, inputs.CFG4_ROWSUM_WIDE.numel)
+    xs = dev_arrays[key4].view(4, -1)                       # 4 rows of 2^26: the split-row path
+    rows_out = torch.empty(4, dtype=torch.float32, device=dev)
+    ms = time_launches(lambda: abi.rdx_rowsum_f32(xs, out=rows_out, stream=stream), iters)
+    extras["rowsum_4x67108864_split"] = {"us": round(ms * 1e3, 2), "GB/s": round((1 << 30) / (ms * 1e-3) / 1e9, 1),
+                                         "bytes": 1 << 30}
+
     # ---- ladder (the page's five block reductions) on the fp32 array --------
     ladder = {}
     x2 = dev_arrays[(inputs.CFG2_SUM_F32.dist, inputs.CFG2_SUM_F32.seed, inputs.CFG2_SUM_F32.numel)]
@@ -437,6 +472,7 @@ def run_gb300(args):
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
         "ladder_fp32_n2^24+13": ladder,
+        "extras": extras,
         "kernel_source_hash": src_hash,
     }
     if rank == 0 and world == 1:

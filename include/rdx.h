@@ -21,12 +21,14 @@
  *  - Sizes are element counts (int64_t); no size limit beyond device memory.
  *  - Any element-aligned input pointer is accepted; 16-byte alignment is not
  *    required.  The output must not overlap the input.
- *  - Scratch: the scalar reductions keep one small workspace per (device,
- *    stream) pair (block partials and a completion counter), allocated by the
- *    library with cudaMalloc on the first call on that pair and reused after.
- *    Make that first call outside any CUDA-graph capture.  Two host threads
- *    may call concurrently; calls on one stream are ordered by the stream.
- *    rdx_shutdown() frees the workspaces.
+ *  - Scratch: the scalar reductions (and the row sum of few, very long rows)
+ *    keep one small workspace per (device, stream) pair (tile partials and
+ *    completion counters, rdx_workspace_bytes() bytes), allocated by the
+ *    library with cudaMalloc on the first call on that pair that needs it and
+ *    reused after.  Make that first call outside any CUDA-graph capture, or
+ *    pass a workspace of your own to rdx_reduce_ws.  Two host threads may
+ *    call concurrently; calls on one stream are ordered by the stream.
+ *    rdx_shutdown() frees the library's workspaces.
  *  - Errors: no exception crosses this ABI.  Each call returns an rdx_status;
  *    argument errors are found before any CUDA call and nothing is enqueued.
  *    After RDX_ERR_CUDA, rdx_last_cuda_error() names the failing CUDA call.
@@ -62,6 +64,15 @@ typedef int rdx_status;
 /* bfloat16 values are passed as their raw 16-bit patterns (the upper half of
  * the IEEE binary32 with the same value). */
 typedef uint16_t rdx_bf16;
+
+/* Scalar reductions by code, for rdx_reduce_ws. */
+#define RDX_OP_SUM_F32 0         /* float in, float out              */
+#define RDX_OP_SUMSQ_F32 1       /* float in, float out              */
+#define RDX_OP_SUM_BF16 2        /* rdx_bf16 in, float out           */
+#define RDX_OP_SUMSQ_BF16 3      /* rdx_bf16 in, float out           */
+#define RDX_OP_SUM_I32 4         /* int32_t in, int64_t out          */
+#define RDX_OP_SUM_SUMSQ_F32 5   /* float in, float[2] out           */
+#define RDX_OP_SUM_SUMSQ_BF16 6  /* rdx_bf16 in, float[2] out        */
 
 /*
  * rdx_sum_f32: *out = sum_{i<n} x[i].
@@ -129,12 +140,45 @@ rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, 
  *   rows  >= 0; rows == 0 enqueues nothing
  *   cols  >= 0; cols == 0 writes rows zeros
  *   out   rows float32 values; must not overlap x
- * Each row is summed by one group of threads in a fixed order, with no
- * workspace and no cross-block step.
+ * Short and medium rows are summed by a group of threads each, long rows by
+ * a block each, with no workspace.  Few, very long rows (fewer than two
+ * waves of blocks, at least 16384 columns, at most 2048 rows) are each cut
+ * into tiles over many blocks and finished on the device like the scalar
+ * sums; that path uses the (device, stream) workspace.  Either way a row's
+ * summation order is fixed by its address and length.
  * Errors: RDX_ERR_INVALID_ARG for negative sizes, rows*cols overflowing
- * int64, NULL or misaligned pointers, overlap.
+ * int64, NULL or misaligned pointers, overlap; RDX_ERR_ALLOC if the split
+ * path's workspace cannot be allocated.
  */
 rdx_status rdx_rowsum_f32(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream);
+
+/*
+ * rdx_rowsum_strided_f32: out[r] = sum_{j<cols} x[r*ld + j] for r < rows:
+ * rdx_rowsum_f32 for rows that start every ld elements (a leading dimension,
+ * e.g. a column slice of a wider row-major matrix).  ld >= cols when
+ * rows > 1; rows need not be 16-byte aligned.  Other arguments, behaviour
+ * and errors as rdx_rowsum_f32.
+ */
+rdx_status rdx_rowsum_strided_f32(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
+                                  cudaStream_t stream);
+
+/* Bytes of a caller-owned workspace for rdx_reduce_ws (a constant). */
+size_t rdx_workspace_bytes(void);
+
+/*
+ * rdx_reduce_ws: the scalar reduction `op` (an RDX_OP_* code) of n elements
+ * of x into out, with a workspace the caller owns instead of the library's.
+ * Results are the same as the named entry point's (same kernel and tiling).
+ *   workspace       device memory of at least rdx_workspace_bytes() bytes,
+ *                   256-byte aligned, zero-filled once before its first use
+ *                   (every call leaves it ready for the next)
+ * The call allocates nothing.  Calls sharing one workspace must be ordered
+ * (one stream, or synchronised): kernels that overlap on the GPU race on it.
+ * Errors: as the named entry point, plus RDX_ERR_INVALID_ARG for a bad op,
+ * a NULL, small or misaligned workspace, or a workspace overlapping x or out.
+ */
+rdx_status rdx_reduce_ws(int op, const void* x, int64_t n, void* out, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
 
 /*
  * rdx_ladder_partials_f32: the page's five block-reduction versions, run as

@@ -60,6 +60,11 @@ def load(path: str = LIB) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [vp, i64, vp, vp], i32
         lib.rdx_rowsum_f32.argtypes, lib.rdx_rowsum_f32.restype = [vp, i64, i64, vp, vp], i32
+        lib.rdx_rowsum_strided_f32.argtypes = [vp, i64, i64, i64, vp, vp]
+        lib.rdx_rowsum_strided_f32.restype = i32
+        lib.rdx_workspace_bytes.argtypes, lib.rdx_workspace_bytes.restype = [], ctypes.c_size_t
+        lib.rdx_reduce_ws.argtypes = [i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
+        lib.rdx_reduce_ws.restype = i32
         lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
@@ -162,6 +167,59 @@ def rdx_rowsum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None
     with torch.cuda.device(x.device):
         st = lib.rdx_rowsum_f32(x.data_ptr(), rows, cols, out.data_ptr(), _stream_handle(stream, x.device))
     _check("rdx_rowsum_f32", st)
+    return out
+
+
+def rdx_rowsum_strided_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """(rows,) float32 tensor: per-row sums of a 2-D float32 tensor whose rows
+    are contiguous (stride(1) == 1) and start every stride(0) elements, such
+    as a column slice of a wider matrix."""
+    lib = load()
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32 or x.dim() != 2:
+        raise TypeError("rdx_rowsum_strided_f32: expected a 2-D float32 CUDA tensor")
+    rows, cols = x.shape
+    if cols > 1 and x.stride(1) != 1:
+        raise ValueError("rdx_rowsum_strided_f32: rows must be contiguous (stride(1) == 1)")
+    ld = x.stride(0) if rows > 1 else cols
+    out = _output(out, x, torch.float32, (rows,))
+    with torch.cuda.device(x.device):
+        st = lib.rdx_rowsum_strided_f32(x.data_ptr(), rows, cols, ld, out.data_ptr(),
+                                        _stream_handle(stream, x.device))
+    _check("rdx_rowsum_strided_f32", st)
+    return out
+
+
+# RDX_OP_* codes of include/rdx.h, by operation name.
+OP_CODES = {"sum_f32": 0, "sumsq_f32": 1, "sum_bf16": 2, "sumsq_bf16": 3, "sum_i32": 4,
+            "sum_sumsq_f32": 5, "sum_sumsq_bf16": 6}
+_OP_IN = {0: (torch.float32,), 1: (torch.float32,), 2: _BF16, 3: _BF16, 4: (torch.int32,), 5: (torch.float32,),
+          6: _BF16}
+_OP_OUT = {0: (torch.float32, ()), 1: (torch.float32, ()), 2: (torch.float32, ()), 3: (torch.float32, ()),
+           4: (torch.int64, ()), 5: (torch.float32, (2,)), 6: (torch.float32, (2,))}
+
+
+def rdx_workspace_bytes() -> int:
+    return int(load().rdx_workspace_bytes())
+
+
+def rdx_reduce_ws(op, x: torch.Tensor, workspace: torch.Tensor, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Scalar reduction ``op`` (a name of OP_CODES or an RDX_OP_* code) with a
+    caller-owned workspace (a CUDA tensor of at least rdx_workspace_bytes()
+    bytes, zero-filled before its first use)."""
+    lib = load()
+    code = OP_CODES[op] if isinstance(op, str) else int(op)
+    if code not in _OP_IN:
+        raise ValueError(f"rdx_reduce_ws: unknown op {op}")
+    x = _input(x, _OP_IN[code], "rdx_reduce_ws")
+    dt, shape = _OP_OUT[code]
+    out = _output(out, x, dt, shape)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("rdx_reduce_ws: workspace must be a contiguous CUDA tensor")
+    with torch.cuda.device(x.device):
+        st = lib.rdx_reduce_ws(code, x.data_ptr(), x.numel(), out.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream, x.device))
+    _check("rdx_reduce_ws", st)
     return out
 
 

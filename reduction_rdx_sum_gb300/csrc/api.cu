@@ -1,6 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/rdx.h: argument
 // validation (before any CUDA call), device capability cache, per-(device,
-// stream) workspace cache, grid choice and launch.
+// stream) workspace cache, choice of kernel and launch.
 #include "rdx.h"
 
 #include <climits>
@@ -28,8 +28,11 @@ std::mutex g_mu;
 std::map<int, DeviceCaps> g_caps;                          // by device ordinal
 std::map<std::pair<int, uintptr_t>, void*> g_workspaces;  // by (device, stream)
 
-// Workspace layout: [completion counter, padded to 256 B][tile partials].
-constexpr size_t kCounterBytes = 256;
+// Workspace layout: [completion counters: one per row, kMaxSplitRows of them]
+// [tile partials: reduce_max_partials() slots of 8 bytes].  The counters must
+// be zero before a launch; every launch leaves them zero.
+constexpr size_t kCounterBytes = size_t(rdx::kMaxSplitRows) * sizeof(unsigned);
+static_assert(kCounterBytes % 256 == 0, "partials start 256-byte aligned");
 
 size_t workspace_bytes() { return kCounterBytes + size_t(rdx::reduce_max_partials()) * 8; }
 
@@ -67,7 +70,7 @@ rdx_status current_device(const DeviceCaps** out) {
     return RDX_OK;
 }
 
-// The (device, stream) workspace; allocated and its counter zeroed (in
+// The (device, stream) workspace; allocated and its counters zeroed (in
 // stream order) on first use.
 rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -92,36 +95,75 @@ rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** o
     e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
     if (e != cudaSuccess) {
         cudaFree(p);
-        return fail_cuda("cudaMemsetAsync of the completion counter", e);
+        return fail_cuda("cudaMemsetAsync of the completion counters", e);
     }
     g_workspaces.emplace(key, p);
     *out = p;
     return RDX_OK;
 }
 
-rdx_status reduce_entry(Op op, const void* x, int64_t n, void* out, cudaStream_t stream) {
-    t_last_error.clear();
+bool valid_op(int op) { return op >= 0 && op < int(Op::kCount); }
+
+// Checks shared by the scalar reductions.
+rdx_status check_scalar(Op op, const void* x, int64_t n, const void* out) {
     const size_t es = rdx::reduce_elem_bytes(op), os = rdx::reduce_acc_bytes(op);
     if (n < 0 || out == nullptr || (n > 0 && x == nullptr)) return RDX_ERR_INVALID_ARG;
     if (n > INT64_MAX / 16) return RDX_ERR_INVALID_ARG;
     if (!is_aligned(x, es) || !is_aligned(out, os)) return RDX_ERR_INVALID_ARG;
     if (overlaps(x, size_t(n) * es, out, os)) return RDX_ERR_INVALID_ARG;
+    return RDX_OK;
+}
+
+// One row of n elements; ws is the workspace (NULL when the plan has one tile).
+rdx_status launch_scalar(Op op, const void* x, int64_t n, void* out, void* ws, cudaStream_t stream) {
+    const rdx::ReducePlan plan = rdx::reduce_plan(op, 1, n);
+    unsigned* counters = static_cast<unsigned*>(ws);
+    void* partials = ws ? static_cast<char*>(ws) + kCounterBytes : nullptr;
+    const cudaError_t e = rdx::reduce_launch(op, x, 1, n, n, plan, partials, counters, out, stream);
+    if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
+    return RDX_OK;
+}
+
+rdx_status reduce_entry(Op op, const void* x, int64_t n, void* out, cudaStream_t stream) {
+    t_last_error.clear();
+    rdx_status st = check_scalar(op, x, n, out);
+    if (st != RDX_OK) return st;
+    const DeviceCaps* dev = nullptr;
+    if ((st = current_device(&dev)) != RDX_OK) return st;
+    void* ws = nullptr;
+    if (rdx::reduce_plan(op, 1, n).tiles > 1 && (st = stream_workspace(*dev, stream, &ws)) != RDX_OK) return st;
+    return launch_scalar(op, x, n, out, ws, stream);
+}
+
+rdx_status rowsum_entry(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
+    t_last_error.clear();
+    if (rows < 0 || cols < 0 || ld < 0) return RDX_ERR_INVALID_ARG;
+    if (rows > 1 && ld < cols) return RDX_ERR_INVALID_ARG;
+    if (rows > INT64_MAX / 16 || cols > INT64_MAX / 16 || ld > INT64_MAX / 16) return RDX_ERR_INVALID_ARG;
+    if (rows > 1 && rows - 1 > (INT64_MAX / 16 - cols) / (ld > 0 ? ld : 1)) return RDX_ERR_INVALID_ARG;
+    if (rows > 0 && out == nullptr) return RDX_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && x == nullptr) return RDX_ERR_INVALID_ARG;
+    if (!is_aligned(x, 4) || !is_aligned(out, 4)) return RDX_ERR_INVALID_ARG;
+    const size_t span = rows > 0 && cols > 0 ? (size_t(rows - 1) * size_t(ld) + size_t(cols)) * 4 : 0;
+    if (overlaps(x, span, out, size_t(rows) * 4)) return RDX_ERR_INVALID_ARG;
+    if (rows == 0) return RDX_OK;
 
     const DeviceCaps* dev = nullptr;
     rdx_status st = current_device(&dev);
     if (st != RDX_OK) return st;
-
-    const rdx::ReducePlan plan = rdx::reduce_plan(op, x, n);
-    unsigned* counter = nullptr;
-    void* partials = nullptr;
-    if (plan.grid > 1) {
+    if (rdx::rowsum_use_split(*dev, rows, cols)) {
+        // few long rows: each row over many blocks (tiles + a per-row finish)
+        const rdx::ReducePlan plan = rdx::reduce_plan(Op::SumF32, rows, cols);
         void* ws = nullptr;
         if ((st = stream_workspace(*dev, stream, &ws)) != RDX_OK) return st;
-        counter = static_cast<unsigned*>(ws);
-        partials = static_cast<char*>(ws) + kCounterBytes;
+        const cudaError_t e =
+            rdx::reduce_launch(Op::SumF32, x, rows, cols, ld, plan, static_cast<char*>(ws) + kCounterBytes,
+                               static_cast<unsigned*>(ws), out, stream);
+        if (e != cudaSuccess) return fail_cuda("split-row kernel launch", e);
+        return RDX_OK;
     }
-    const cudaError_t e = rdx::reduce_launch(op, x, n, plan, partials, counter, out, stream);
-    if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
+    const cudaError_t e = rdx::rowsum_launch(*dev, x, rows, cols, ld, out, stream);
+    if (e != cudaSuccess) return fail_cuda("rowsum kernel launch", e);
     return RDX_OK;
 }
 
@@ -159,23 +201,31 @@ rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, 
     return reduce_entry(Op::SumSumSqBF16, x, n, out2, stream);
 }
 
-rdx_status rdx_rowsum_f32(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
-    t_last_error.clear();
-    if (rows < 0 || cols < 0) return RDX_ERR_INVALID_ARG;
-    if (cols > 0 && rows > INT64_MAX / 16 / cols) return RDX_ERR_INVALID_ARG;
-    if (rows > INT64_MAX / 16) return RDX_ERR_INVALID_ARG;
-    if (rows > 0 && out == nullptr) return RDX_ERR_INVALID_ARG;
-    if (rows > 0 && cols > 0 && x == nullptr) return RDX_ERR_INVALID_ARG;
-    if (!is_aligned(x, 4) || !is_aligned(out, 4)) return RDX_ERR_INVALID_ARG;
-    if (overlaps(x, size_t(rows) * size_t(cols) * 4, out, size_t(rows) * 4)) return RDX_ERR_INVALID_ARG;
-    if (rows == 0) return RDX_OK;
+size_t rdx_workspace_bytes(void) { return workspace_bytes(); }
 
-    const DeviceCaps* dev = nullptr;
-    const rdx_status st = current_device(&dev);
+rdx_status rdx_reduce_ws(int op, const void* x, int64_t n, void* out, void* workspace, size_t workspace_size,
+                         cudaStream_t stream) {
+    t_last_error.clear();
+    if (!valid_op(op)) return RDX_ERR_INVALID_ARG;
+    rdx_status st = check_scalar(Op(op), x, n, out);
     if (st != RDX_OK) return st;
-    const cudaError_t e = rdx::rowsum_launch(*dev, x, rows, cols, out, stream);
-    if (e != cudaSuccess) return fail_cuda("rowsum kernel launch", e);
-    return RDX_OK;
+    if (workspace == nullptr || workspace_size < workspace_bytes() || !is_aligned(workspace, 256))
+        return RDX_ERR_INVALID_ARG;
+    const size_t es = rdx::reduce_elem_bytes(Op(op)), os = rdx::reduce_acc_bytes(Op(op));
+    if (overlaps(workspace, workspace_bytes(), x, size_t(n) * es) || overlaps(workspace, workspace_bytes(), out, os))
+        return RDX_ERR_INVALID_ARG;
+    const DeviceCaps* dev = nullptr;
+    if ((st = current_device(&dev)) != RDX_OK) return st;
+    return launch_scalar(Op(op), x, n, out, workspace, stream);
+}
+
+rdx_status rdx_rowsum_f32(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
+    return rowsum_entry(x, rows, cols, cols, out, stream);
+}
+
+rdx_status rdx_rowsum_strided_f32(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
+                                  cudaStream_t stream) {
+    return rowsum_entry(x, rows, cols, ld, out, stream);
 }
 
 int64_t rdx_ladder_num_partials(int version, int64_t n) {

@@ -22,14 +22,14 @@ struct DeviceCaps {
     int rowsum_group_bps = 0;  // resident blocks per SM of the short-row kernel
 };
 
-// ---- scalar reductions (reduce.cu) ----------------------------------------
-// How one call is cut: `head` elements before the first 16-byte boundary of x,
-// then tiles of `tile` 16-byte vectors, one block each (`grid` blocks, at most
-// reduce_max_partials()).  Depends only on n and x's alignment.
+// ---- tiled reductions (reduce.cu) -----------------------------------------
+// One call sums `rows` segments of `cols` elements, segment r starting at
+// x + r * ld (the scalar reductions: rows = 1).  Each row is cut into `tiles`
+// tiles of `tile` 16-byte vectors, one block each; the plan depends only on
+// rows and cols.  rows * tiles <= reduce_max_partials() for rows <= that.
 struct ReducePlan {
-    int64_t head = 0;
     int64_t tile = 0;
-    int64_t grid = 1;
+    int64_t tiles = 1;
 };
 int reduce_block_threads();
 int reduce_unroll();
@@ -37,16 +37,22 @@ int64_t reduce_max_partials();
 int reduce_vec_elems(Op op);
 size_t reduce_elem_bytes(Op op);
 size_t reduce_acc_bytes(Op op);
-ReducePlan reduce_plan(Op op, const void* x, int64_t n);
-// partials: plan.grid accumulator slots (reduce_acc_bytes each); counter: a
-// zeroed completion counter.  Neither is touched when plan.grid == 1.
-cudaError_t reduce_launch(Op op, const void* x, int64_t n, const ReducePlan& plan, void* partials,
-                          unsigned* counter, void* out, cudaStream_t stream);
+ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols);
+// partials: rows * plan.tiles slots (reduce_acc_bytes each); counters: rows
+// zeroed completion counters, left zeroed.  Neither is touched when
+// plan.tiles == 1.  out: rows results.
+cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
+                          void* partials, unsigned* counters, void* out, cudaStream_t stream);
 
 // ---- row-segmented sum (rowsum.cu) ----------------------------------------
 cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps);
-cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+// Rows of `cols` elements starting every `ld` elements; no workspace.
+cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
                           cudaStream_t stream);
+// Whether a (rows, cols) matrix is better summed by the tiled reduce kernel
+// (few, long rows: each row split over many blocks).
+bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols);
+constexpr int64_t kMaxSplitRows = 2048;
 
 // ---- error text shared by every entry point (api.cu) ------------------------
 // Replace the calling thread's rdx_last_cuda_error() text.

@@ -110,16 +110,16 @@ extern "C" rdx_status rdx_sum_f32_noalloc(const float* x, int64_t n, float* out,
     rdx_status st = setup_current_device(&s);
     if (st != RDX_OK) return st;
 
-    const rdx::ReducePlan plan = rdx::reduce_plan(rdx::Op::SumF32, x, n);
-    if (plan.grid > kMaxPartials)
-        return fail(RDX_ERR_INVALID_ARG, "rdx_sum_f32_noalloc: this launch needs " + std::to_string(plan.grid) +
+    const rdx::ReducePlan plan = rdx::reduce_plan(rdx::Op::SumF32, 1, n);
+    if (plan.tiles > kMaxPartials)
+        return fail(RDX_ERR_INVALID_ARG, "rdx_sum_f32_noalloc: this launch needs " + std::to_string(plan.tiles) +
                                              " block partials; the static scratch holds " +
                                              std::to_string(kMaxPartials));
 
     unsigned char* scratch = static_cast<unsigned char*>(s->scratch);
     cudaError_t e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
     if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync of the completion counter", e);
-    e = rdx::reduce_launch(rdx::Op::SumF32, x, n, plan, scratch + kCounterBytes,
+    e = rdx::reduce_launch(rdx::Op::SumF32, x, 1, n, n, plan, scratch + kCounterBytes,
                            reinterpret_cast<unsigned*>(scratch), out, stream);
     if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
     return RDX_OK;

@@ -20,8 +20,12 @@
 //     last at a completion counter (acquire-release atomic) adds all partials
 //     in a fixed order and resets the counter.  Nothing waits on anything,
 //     and no float atomics are used.
-// The tiling depends only on n and the input's 16-byte alignment, so the
-// summation order, and the result, are the same on every run and every GPU.
+// The same kernel sums the rows of a matrix with few, long rows: gridDim.y
+// rows, each cut into tiles with its own completion counter and partials;
+// the scalar reductions are the one-row case.
+// The tiling depends only on the row length and the row's 16-byte alignment,
+// so the summation order, and the result, are the same on every run and
+// every GPU.
 #include "device.cuh"
 #include "launch.h"
 
@@ -43,7 +47,7 @@ namespace {
 
 constexpr int kBlock = RDX_REDUCE_BLOCK;                  // threads per block
 constexpr int kUnroll = RDX_REDUCE_UNROLL;                // 16-byte loads in flight per thread
-constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // upper bound on blocks (= partials)
+constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // tiles (= partials) aimed at per call
 constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per tile, at least
 constexpr int kFinishLoadBytes = 32;                      // partial bytes in flight per thread, last block
 // 8 resident blocks of 256 threads fill an SM (2048 threads): at most 32
@@ -66,18 +70,25 @@ __device__ __forceinline__ unsigned take_ticket(unsigned* counter) {
 
 template <class P>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSm)
-reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head, int64_t tile,
-              typename P::Acc* __restrict__ partials, unsigned* __restrict__ counter,
+reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, int64_t tile,
+              typename P::Acc* __restrict__ partials, unsigned* __restrict__ counters,
               typename P::Acc* __restrict__ out) {
     using Acc = typename P::Acc;
     constexpr int V = P::kVec;
     __shared__ Acc smem[kBlock / kWarpSize];
     __shared__ unsigned last_block;
 
-    const int64_t m = (n - head) / V;  // whole 16-byte vectors after the head
+    // This block's row and tile.  head = elements before the row's first
+    // 16-byte boundary, then m whole 16-byte vectors, then the tail.
+    const int64_t row = blockIdx.y;
+    const typename P::In* __restrict__ xr = x + row * ld;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(xr) & 15u;
+    int64_t head = mis ? int64_t((16u - mis) / sizeof(typename P::In)) : 0;
+    if (head > cols) head = cols;
+    const int64_t m = (cols - head) / V;
     const int64_t t0 = int64_t(blockIdx.x) * tile;
     const int64_t t1 = t0 + tile < m ? t0 + tile : m;
-    const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(x + head);
+    const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(xr + head);
 
     // accumulator of load slot u: its own for float sums, a shared one for
     // exact (integer) sums
@@ -88,11 +99,11 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head, int
     for (int u = 0; u < kUnroll; ++u) acc[u] = Acc(0);
 
     // Fewer than V elements before the first 16-byte boundary and after the
-    // last whole vector: the first threads of block 0 take one each.
+    // last whole vector: the first threads of the row's tile 0 take one each.
     if (blockIdx.x == 0) {
         const int64_t tail0 = head + m * V;
-        if (threadIdx.x < head) acc[0] += P::term(x[threadIdx.x]);
-        if (threadIdx.x < n - tail0) acc[kUnroll - 1] += P::term(x[tail0 + threadIdx.x]);
+        if (threadIdx.x < head) acc[0] += P::term(xr[threadIdx.x]);
+        if (threadIdx.x < cols - tail0) acc[kUnroll - 1] += P::term(xr[tail0 + threadIdx.x]);
     }
 
     int64_t i = t0 + threadIdx.x;
@@ -113,19 +124,21 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head, int
     Acc a = block_sum<kBlock>(fold_array(acc), smem);
 
     if (gridDim.x == 1) {
-        if (threadIdx.x == 0) *out = a;
+        if (threadIdx.x == 0) out[row] = a;
         return;
     }
+    Acc* __restrict__ rp = partials + row * int64_t(gridDim.x);
+    unsigned* counter = counters + row;
     if (threadIdx.x == 0) {
-        partials[blockIdx.x] = a;
+        rp[blockIdx.x] = a;
         last_block = take_ticket(counter) == gridDim.x - 1;
     }
     __syncthreads();
     if (!last_block) return;
 
-    // The last block: every partial is in place.  Thread t adds partials
-    // t, t + kBlock, ... (kFinishUnroll independent chains, loads in flight
-    // together), then the block tree.
+    // The row's last block: every partial of the row is in place.  Thread t
+    // adds partials t, t + kBlock, ... (kFinishUnroll independent chains,
+    // loads in flight together), then the block tree.
     constexpr int kFinishUnroll = kFinishLoadBytes / int(sizeof(Acc));
     Acc b[kFinishUnroll];
 #pragma unroll
@@ -135,27 +148,28 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t n, int64_t head, int
     for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
         Acc p[kFinishUnroll];
 #pragma unroll
-        for (int u = 0; u < kFinishUnroll; ++u) p[u] = load_cg(partials + j + u * kBlock);
+        for (int u = 0; u < kFinishUnroll; ++u) p[u] = load_cg(rp + j + u * kBlock);
 #pragma unroll
         for (int u = 0; u < kFinishUnroll; ++u) b[u] += p[u];
     }
 #pragma unroll
     for (int u = 0; u < kFinishUnroll; ++u) {
-        if (j + u * kBlock < g) b[u] += load_cg(partials + j + u * kBlock);
+        if (j + u * kBlock < g) b[u] += load_cg(rp + j + u * kBlock);
     }
     const Acc total = block_sum<kBlock>(fold_array(b), smem);
     if (threadIdx.x == 0) {
-        *out = total;
+        out[row] = total;
         *counter = 0u;  // ready for the next call on this stream
     }
 }
 
 template <class P>
-cudaError_t launch_typed(const void* x, int64_t n, const ReducePlan& plan, void* partials, unsigned* counter,
-                         void* out, cudaStream_t stream) {
-    reduce_kernel<P><<<unsigned(plan.grid), kBlock, 0, stream>>>(
-        static_cast<const typename P::In*>(x), n, plan.head, plan.tile, static_cast<typename P::Acc*>(partials),
-        counter, static_cast<typename P::Acc*>(out));
+cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
+                         void* partials, unsigned* counters, void* out, cudaStream_t stream) {
+    const dim3 grid(unsigned(plan.tiles), unsigned(rows));
+    reduce_kernel<P><<<grid, kBlock, 0, stream>>>(static_cast<const typename P::In*>(x), cols, ld, plan.tile,
+                                                  static_cast<typename P::Acc*>(partials), counters,
+                                                  static_cast<typename P::Acc*>(out));
     return cudaGetLastError();
 }
 
@@ -163,6 +177,7 @@ cudaError_t launch_typed(const void* x, int64_t n, const ReducePlan& plan, void*
 
 int reduce_block_threads() { return kBlock; }
 int reduce_unroll() { return kUnroll; }
+// rows * tiles <= kMaxTiles for any rows <= kMaxTiles (see reduce_plan)
 int64_t reduce_max_partials() { return kMaxTiles; }
 
 int reduce_vec_elems(Op op) {
@@ -180,32 +195,32 @@ size_t reduce_acc_bytes(Op op) {
     return (op == Op::SumI32 || op == Op::SumSumSqF32 || op == Op::SumSumSqBF16) ? 8 : 4;
 }
 
-ReducePlan reduce_plan(Op op, const void* x, int64_t n) {
+ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     ReducePlan p;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(x) & 15u;
-    p.head = mis ? int64_t((16u - mis) / reduce_elem_bytes(op)) : 0;
-    if (p.head > n) p.head = n;
-    const int64_t m = (n - p.head) / reduce_vec_elems(op);
-    int64_t tile = (m + kMaxTiles - 1) / kMaxTiles;
+    const int64_t mmax = cols / reduce_vec_elems(op);  // whole vectors of a row, at most
+    const int64_t target = kMaxTiles / (rows > 0 ? rows : 1);
+    int64_t tile = (mmax + target - 1) / (target > 0 ? target : 1);
     tile = (tile + kBlock - 1) / kBlock * kBlock;  // whole blocks of vectors
     if (tile < kMinTile) tile = kMinTile;
     p.tile = tile;
-    p.grid = m > 0 ? (m + tile - 1) / tile : 1;  // <= kMaxTiles
+    p.tiles = mmax > 0 ? (mmax + tile - 1) / tile : 1;
     return p;
 }
 
-cudaError_t reduce_launch(Op op, const void* x, int64_t n, const ReducePlan& plan, void* partials,
-                          unsigned* counter, void* out, cudaStream_t stream) {
+cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
+                          void* partials, unsigned* counters, void* out, cudaStream_t stream) {
+#define RDX_LAUNCH(P) launch_typed<P>(x, rows, cols, ld, plan, partials, counters, out, stream)
     switch (op) {
-        case Op::SumF32: return launch_typed<SumF32>(x, n, plan, partials, counter, out, stream);
-        case Op::SumSqF32: return launch_typed<SumSqF32>(x, n, plan, partials, counter, out, stream);
-        case Op::SumBF16: return launch_typed<SumBF16>(x, n, plan, partials, counter, out, stream);
-        case Op::SumSqBF16: return launch_typed<SumSqBF16>(x, n, plan, partials, counter, out, stream);
-        case Op::SumI32: return launch_typed<SumI32>(x, n, plan, partials, counter, out, stream);
-        case Op::SumSumSqF32: return launch_typed<SumSumSqF32>(x, n, plan, partials, counter, out, stream);
-        case Op::SumSumSqBF16: return launch_typed<SumSumSqBF16>(x, n, plan, partials, counter, out, stream);
+        case Op::SumF32: return RDX_LAUNCH(SumF32);
+        case Op::SumSqF32: return RDX_LAUNCH(SumSqF32);
+        case Op::SumBF16: return RDX_LAUNCH(SumBF16);
+        case Op::SumSqBF16: return RDX_LAUNCH(SumSqBF16);
+        case Op::SumI32: return RDX_LAUNCH(SumI32);
+        case Op::SumSumSqF32: return RDX_LAUNCH(SumSumSqF32);
+        case Op::SumSumSqBF16: return RDX_LAUNCH(SumSumSqBF16);
         default: return cudaErrorInvalidValue;
     }
+#undef RDX_LAUNCH
 }
 
 }  // namespace rdx

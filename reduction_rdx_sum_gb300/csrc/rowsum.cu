@@ -12,8 +12,10 @@
 //     the row four vectors per lane at a time;
 //   * long rows: one block per row, the same add-on-load loop and block tree
 //     as the scalar reduction, a direct store of the row's sum.
-// A row's summation order depends only on its address and length, never on
-// the grid, so the result is bitwise reproducible.  No workspace is needed.
+// Rows may start every ld >= cols elements (a leading dimension).  A row's
+// summation order depends only on its address and length, never on the grid,
+// so the result is bitwise reproducible.  No workspace is needed.  (Few, very
+// long rows go to the tiled kernel of reduce.cu instead; see rowsum_use_split.)
 #include "device.cuh"
 #include "launch.h"
 
@@ -70,7 +72,8 @@ __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_
 // The NG rows of one warp step are consecutive, so are their sums.
 template <int LPR>
 __global__ void __launch_bounds__(kGroupBlock)
-rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
+rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                    float* __restrict__ out) {
     constexpr int NG = kWarpSize / LPR;  // rows in flight per warp step
     const int lane = threadIdx.x % kWarpSize;
     const int grp = lane / LPR;
@@ -81,7 +84,7 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, flo
     for (int64_t k = warp; k < nsteps; k += nwarps) {
         const int64_t r = k * NG + grp;
         float s = 0.f;
-        if (r < rows) s = row_share<LPR>(x + r * cols, cols, l);
+        if (r < rows) s = row_share<LPR>(x + r * ld, cols, l);
         s = group_allreduce<LPR>(s);  // every lane takes part, in range or not
         if (l == 0 && r < rows) out[r] = s;
     }
@@ -93,7 +96,8 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, flo
 // before the first reduction.  Lane 0 of each group stores its row's sum.
 template <int LPR>
 __global__ void __launch_bounds__(kGroupBlock)
-rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
+rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                  float* __restrict__ out) {
     constexpr int NG = kWarpSize / LPR;
     constexpr int RU = NG * kRowSteps;  // rows per unit
     const int lane = threadIdx.x % kWarpSize;
@@ -112,7 +116,7 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float
 #pragma unroll
             for (int u = 0; u < 4; ++u) v[q * 4 + u] = make_uint4(0u, 0u, 0u, 0u);
             if (r < rows) {
-                const float* __restrict__ row = x + r * cols;
+                const float* __restrict__ row = x + r * ld;
                 const int64_t head = row_head(row, cols);
                 const int64_t m = (cols - head) >> 2;
                 const int64_t tail0 = head + 4 * m;
@@ -141,11 +145,11 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float
 
 // Long rows: one block per row (a block loops over rows r, r + gridDim.x, ...).
 __global__ void __launch_bounds__(kCtaBlock)
-rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, float* __restrict__ out) {
+rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, float* __restrict__ out) {
     __shared__ float smem[kCtaBlock / kWarpSize];
     const int t = threadIdx.x;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const float* __restrict__ row = x + r * cols;
+        const float* __restrict__ row = x + r * ld;
         const int64_t head = row_head(row, cols);
         const int64_t m = (cols - head) >> 2;
         const int64_t tail0 = head + 4 * m;
@@ -184,7 +188,7 @@ int lanes_per_row(int64_t cols) {
 }
 
 template <int LPR>
-cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
                        cudaStream_t stream) {
     constexpr int64_t kRU = (kWarpSize / LPR) * kRowSteps;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
@@ -193,12 +197,12 @@ cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int6
     // four waves of resident blocks; each warp then loops over its units
     const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
     if (blocks > cap) blocks = cap;
-    rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, out);
+    rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
 
 template <int LPR>
-cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
                          cudaStream_t stream) {
     constexpr int64_t kNG = kWarpSize / LPR;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
@@ -207,7 +211,7 @@ cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, in
     // four waves of resident blocks; each warp then loops over its steps
     const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
     if (blocks > cap) blocks = cap;
-    rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, out);
+    rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
 
@@ -219,22 +223,29 @@ cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(group_bps, rowsum_fit_kernel<16>, kGroupBlock, 0);
 }
 
-cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, float* out,
+bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols) {
+    // fewer rows than two waves of one-block-per-row, each long enough for
+    // at least four tiles
+    const int64_t wave = int64_t(dev.sms) * (dev.rowsum_cta_bps > 0 ? dev.rowsum_cta_bps : 1);
+    return rows <= kMaxSplitRows && rows < 2 * wave && cols >= 16384;
+}
+
+cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
                           cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {
-            case 1: return launch_fit<1>(dev, x, rows, cols, out, stream);
-            case 2: return launch_fit<2>(dev, x, rows, cols, out, stream);
-            case 4: return launch_fit<4>(dev, x, rows, cols, out, stream);
-            case 8: return launch_fit<8>(dev, x, rows, cols, out, stream);
-            case 16: return launch_fit<16>(dev, x, rows, cols, out, stream);
-            default: return launch_fit<32>(dev, x, rows, cols, out, stream);
+            case 1: return launch_fit<1>(dev, x, rows, cols, ld, out, stream);
+            case 2: return launch_fit<2>(dev, x, rows, cols, ld, out, stream);
+            case 4: return launch_fit<4>(dev, x, rows, cols, ld, out, stream);
+            case 8: return launch_fit<8>(dev, x, rows, cols, ld, out, stream);
+            case 16: return launch_fit<16>(dev, x, rows, cols, ld, out, stream);
+            default: return launch_fit<32>(dev, x, rows, cols, ld, out, stream);
         }
     }
-    if (cols <= kGroupRowMaxCols) return launch_group<32>(dev, x, rows, cols, out, stream);
+    if (cols <= kGroupRowMaxCols) return launch_group<32>(dev, x, rows, cols, ld, out, stream);
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
-    rowsum_cta_kernel<<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, out);
+    rowsum_cta_kernel<<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
 

@@ -91,3 +91,34 @@ def test_python_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(abi, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         abi.load(str(tmp_path / "missing.so"))
+
+
+def test_workspace_entry_validation(lib):
+    f = lib.rdx_reduce_ws
+    f.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    lib.rdx_workspace_bytes.restype = ctypes.c_size_t
+    wsb = lib.rdx_workspace_bytes()
+    assert wsb >= 256 + 8192 * 8 and wsb % 256 == 0
+    ws = FAKE + (1 << 30)
+    assert f(7, FAKE, 10, FAKE + 4096, ws, wsb, None) == INVALID            # bad op
+    assert f(-1, FAKE, 10, FAKE + 4096, ws, wsb, None) == INVALID
+    assert f(0, FAKE, 10, FAKE + 4096, None, wsb, None) == INVALID          # no workspace
+    assert f(0, FAKE, 10, FAKE + 4096, ws, wsb - 1, None) == INVALID        # too small
+    assert f(0, FAKE, 10, FAKE + 4096, ws + 16, wsb, None) == INVALID       # not 256-byte aligned
+    assert f(0, FAKE, 1 << 20, FAKE + (1 << 23), FAKE + 4096, wsb, None) == INVALID  # workspace inside x
+    assert f(0, FAKE, 10, ws + 64, ws, wsb, None) == INVALID                # out inside workspace
+    assert f(4, FAKE, 10, FAKE + 4096 + 4, ws, wsb, None) == INVALID        # int64 out misaligned
+
+
+def test_strided_rowsum_validation(lib):
+    f = lib.rdx_rowsum_strided_f32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(FAKE, 4, 10, 9, FAKE + 4096, None) == INVALID                  # ld < cols
+    assert f(FAKE, 4, 10, -1, FAKE + 4096, None) == INVALID
+    assert f(FAKE, 4, 10, 20, FAKE + 4 * 65, None) == INVALID               # out inside the last row
+    assert f(FAKE, 1 << 40, 8, 1 << 30, FAKE - 64, None) == INVALID         # span overflows
+    assert f(None, 0, 10, 20, None, None) == abi.RDX_OK

@@ -11,9 +11,9 @@ Contents
 ``oracle.c`` (loaded here through ctypes)
     The plain definitions, one loop in index order each: float64 Kahan sums for
     float32 and bfloat16 inputs, int64 sums for int32, per-row loops for the
-    row-segmented sum.  Page "03_shared_memory_sync_reduction.py", demo 3:
-    the expected value of every reduction version is the float64 sum of the
-    input.
+    row-segmented sum, and the maximum by the page's atomic_max rule.  Page
+    "03_shared_memory_sync_reduction.py", demo 3: the expected value of every
+    reduction version is the float64 sum of the input.
 ``ladder.py``
     The five block-level reduction versions of that page's demo 3, restated in
     numpy float32 in the page's order of operations, giving each block's
@@ -66,6 +66,8 @@ def _load():
         for name in ("oracle_rowsum_f32", "oracle_rowabssum_f32"):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [p, i64, i64, p], None
+        lib.oracle_max_f32.argtypes, lib.oracle_max_f32.restype = [p, i64], ctypes.c_float
+        lib.oracle_max_i32.argtypes, lib.oracle_max_i32.restype = [p, i64], ctypes.c_int32
         _lib = lib
         return lib
 
@@ -125,6 +127,20 @@ def sum_i32(x: np.ndarray) -> int:
     """Exact int64 sum of int32 values."""
     a = _flat(x, np.int32)
     return int(_load().oracle_sum_i32(_ptr(a), a.size))
+
+
+# ---- maximum (the page's atomic_max rule, folded from -Inf) ----------------
+
+def max_f32(x: np.ndarray) -> float:
+    """Largest float32 value; NaNs are ignored, empty or all-NaN gives -Inf."""
+    a = _flat(x, np.float32)
+    return float(_load().oracle_max_f32(_ptr(a), a.size))
+
+
+def max_i32(x: np.ndarray) -> int:
+    """Largest int32 value; empty input gives -2^31."""
+    a = _flat(x, np.int32)
+    return int(_load().oracle_max_i32(_ptr(a), a.size))
 
 
 # ---- row-segmented float32 -------------------------------------------------

@@ -150,3 +150,23 @@ void oracle_rowabssum_f32(const float* x, int64_t rows, int64_t cols, double* ou
         out[r] = kahan_result(&k);
     }
 }
+
+/* ---- maximum ------------------------------------------------------------ */
+
+/* The page "lecture02/simt.py" models atomic_max as: old = A[i]; if v > old
+ * then A[i] = v.  Folding every input through that rule from -Inf gives the
+ * maximum; a NaN is never greater than anything, so it never replaces the
+ * running value (NaNs are ignored; all-NaN or empty input gives -Inf). */
+float oracle_max_f32(const float* x, int64_t n) {
+    float m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i)
+        if (x[i] > m) m = x[i];
+    return m;
+}
+
+int32_t oracle_max_i32(const int32_t* x, int64_t n) {
+    int32_t m = INT32_MIN;
+    for (int64_t i = 0; i < n; ++i)
+        if (x[i] > m) m = x[i];
+    return m;
+}

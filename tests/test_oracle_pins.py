@@ -243,3 +243,40 @@ def test_rowsum_rows_and_orientation():
         e[pos] = 1.0
         out = oracle.rowsum_f32(e.reshape(3, 5))
         assert out.tolist() == [1.0 if r == pos // 5 else 0.0 for r in range(3)]
+
+
+# ---------------------------------------------------------------------------
+# maximum
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 31, 33, 1000, (1 << 16) + 3])
+def test_max_closed_forms_and_impulses(n):
+    assert oracle.max_f32(np.arange(n, dtype=np.float32)) == n - 1
+    assert oracle.max_f32(-np.arange(n, dtype=np.float32)) == 0.0
+    assert oracle.max_i32(np.arange(n, dtype=np.int32) - n) == -1
+    for pos in sorted({0, n // 3, n - 1}):
+        x = np.full(n, -5.0, np.float32)
+        x[pos] = 7.5
+        assert oracle.max_f32(x) == 7.5
+        z = np.full(n, -(2 ** 31), np.int32)
+        z[pos] = 2 ** 31 - 1
+        assert oracle.max_i32(z) == 2 ** 31 - 1
+
+
+def test_max_special_values():
+    nan, inf = np.float32(np.nan), np.float32(np.inf)
+    assert oracle.max_f32(np.zeros(0, np.float32)) == -np.inf
+    assert oracle.max_f32(np.float32([nan, nan])) == -np.inf
+    assert oracle.max_f32(np.float32([nan, 1, nan, -3])) == 1.0      # NaN never wins
+    assert oracle.max_f32(np.float32([-inf, -1e30])) == np.float32(-1e30)
+    assert oracle.max_f32(np.float32([1, inf, 2])) == np.inf
+    assert oracle.max_i32(np.zeros(0, np.int32)) == -(2 ** 31)
+
+
+@pytest.mark.parametrize("n", [1, 7, 64])
+def test_max_brute_force(n):
+    rng = np.random.default_rng(40 + n)
+    x = (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n)).astype(np.float32)
+    assert oracle.max_f32(x) == max(float(v) for v in x)
+    z = rng.integers(-(2 ** 31), 2 ** 31, n, dtype=np.int64).astype(np.int32)
+    assert oracle.max_i32(z) == max(int(v) for v in z)

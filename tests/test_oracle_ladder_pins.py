@@ -4,6 +4,7 @@ integer segment sums, unit impulses (a wrong index or a dropped term moves or
 loses the impulse), the float32 tree error bound, and the page's worked
 example.
 """
+import math
 import os
 from fractions import Fraction
 
@@ -91,3 +92,29 @@ def test_bad_arguments():
     with pytest.raises(ValueError):
         ladder_partials(1, np.zeros(4, np.float32), block=96)
     assert ladder_partials(3, np.zeros(0, np.float32)).shape == (0,)
+
+
+# ---------------------------------------------------------------------------
+# the bank-conflict model of demo 1
+# ---------------------------------------------------------------------------
+
+def test_bank_rounds_match_the_page(golden_dir):
+    from oracle import banks
+
+    with open(os.path.join(golden_dir, "page_demo1_bank_rounds.txt")) as f:
+        table = [tuple(int(v) for v in ln.split()) for ln in f if ln.strip() and not ln.startswith("#")]
+    assert [p for p, _ in table] == list(range(len(banks.PATTERNS)))
+    for p, rounds in table:
+        assert banks.wavefronts(banks.indices(p)) == rounds, banks.PATTERNS[p][0]
+
+
+def test_bank_model_closed_forms():
+    from oracle import banks
+
+    for s in range(1, 65):
+        # stride s: 32 / (32 / gcd(s, 32)) distinct banks -> gcd(s, 32) words per bank
+        words = [s * t for t in range(32)]
+        assert banks.wavefronts(words) == math.gcd(s, 32)
+    assert banks.wavefronts([5] * 32) == 1
+    assert banks.wavefronts([]) == 0
+    assert banks.wavefronts([0, 32, 64, 0]) == 3          # repeats of a word do not count twice

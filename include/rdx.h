@@ -73,6 +73,8 @@ typedef uint16_t rdx_bf16;
 #define RDX_OP_SUM_I32 4         /* int32_t in, int64_t out          */
 #define RDX_OP_SUM_SUMSQ_F32 5   /* float in, float[2] out           */
 #define RDX_OP_SUM_SUMSQ_BF16 6  /* rdx_bf16 in, float[2] out        */
+#define RDX_OP_MAX_F32 7         /* float in, float out              */
+#define RDX_OP_MAX_I32 8         /* int32_t in, int32_t out          */
 
 /*
  * rdx_sum_f32: *out = sum_{i<n} x[i].
@@ -130,6 +132,23 @@ rdx_status rdx_sum_sumsq_f32(const float* x, int64_t n, float* out2, cudaStream_
  * bfloat16 array in one pass, float32 accumulation.  out2 as above.
  */
 rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, cudaStream_t stream);
+
+/*
+ * rdx_max_f32: *out = max_{i<n} x[i].
+ * The page "lecture02/simt.py" models atomic_max as "replace the stored value
+ * when the new one is greater"; folding the input through that rule from
+ * -Inf gives this maximum.  NaNs never win (they are skipped); n == 0 or an
+ * all-NaN input gives -Inf.  The maximum is exact in any grouping, so the
+ * result does not depend on the summation tree (the sign of a zero maximum
+ * is not specified).  Arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_max_f32(const float* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_max_i32: *out = max_{i<n} x[i] for int32 input; n == 0 gives -2^31.
+ * out: one int32, 4-byte aligned.  Arguments and errors as rdx_sum_f32.
+ */
+rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t stream);
 
 /*
  * rdx_rowsum_f32: out[r] = sum_{j<cols} x[r*cols + j] for r < rows.
@@ -229,6 +248,25 @@ int64_t rdx_ladder_num_partials(int version, int64_t n);
  * Arguments and other errors as rdx_sum_f32.
  */
 rdx_status rdx_sum_f32_noalloc(const float* x, int64_t n, float* out, cudaStream_t stream);
+
+/*
+ * rdx_bank_probe: the shared-memory bank-conflict probe of the page
+ * "03_shared_memory_sync_reduction.py", demo 1.  One warp reads one word of
+ * a 32*33-word shared array at index fn(tid) mod 1056, for
+ *   pattern 0..5  stride 1, 2, 4, 8, 16, 32 (tid * stride)
+ *   pattern 6     stride 33        pattern 7  stride 3
+ *   pattern 8     one word (broadcast)        pattern 9  tid / 2
+ * iters * rdx_bank_probe_loads_per_iter() times, and writes the clock cycles
+ * those loads took to *cycles (device memory, 8-byte aligned); sink (32 words
+ * of device memory) receives the loaded data so no load is optimised away.
+ * A conflict of w ways costs about w times the cycles of a conflict-free
+ * access.  Errors: RDX_ERR_INVALID_ARG for a pattern outside 0..9, iters
+ * outside 1..2^20, NULL, misaligned or overlapping outputs.
+ */
+rdx_status rdx_bank_probe(int pattern, int iters, int64_t* cycles, uint32_t* sink, cudaStream_t stream);
+
+/* Loads one iteration of rdx_bank_probe issues. */
+int rdx_bank_probe_loads_per_iter(void);
 
 /* Static text for a status code ("ok", "invalid argument", ...). */
 const char* rdx_status_string(rdx_status status);

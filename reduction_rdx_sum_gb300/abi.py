@@ -56,7 +56,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         for name in ("rdx_sum_f32", "rdx_sumsq_f32", "rdx_sum_bf16_f32acc", "rdx_sumsq_bf16_f32acc",
-                     "rdx_sum_i32_i64", "rdx_sum_sumsq_f32", "rdx_sum_sumsq_bf16_f32acc"):
+                     "rdx_sum_i32_i64", "rdx_sum_sumsq_f32", "rdx_sum_sumsq_bf16_f32acc", "rdx_max_f32",
+                     "rdx_max_i32"):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [vp, i64, vp, vp], i32
         lib.rdx_rowsum_f32.argtypes, lib.rdx_rowsum_f32.restype = [vp, i64, i64, vp, vp], i32
@@ -65,6 +66,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib.rdx_workspace_bytes.argtypes, lib.rdx_workspace_bytes.restype = [], ctypes.c_size_t
         lib.rdx_reduce_ws.argtypes = [i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
         lib.rdx_reduce_ws.restype = i32
+        lib.rdx_bank_probe.argtypes, lib.rdx_bank_probe.restype = [i32, i32, vp, vp, vp], i32
+        lib.rdx_bank_probe_loads_per_iter.argtypes, lib.rdx_bank_probe_loads_per_iter.restype = [], i32
         lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
@@ -156,6 +159,16 @@ def rdx_sum_sumsq_bf16_f32acc(x: torch.Tensor, out: torch.Tensor | None = None, 
     return _scalar("rdx_sum_sumsq_bf16_f32acc", x, _BF16, torch.float32, out, stream, shape=(2,))
 
 
+def rdx_max_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the maximum of a float32 tensor (NaNs skipped; empty gives -Inf)."""
+    return _scalar("rdx_max_f32", x, (torch.float32,), torch.float32, out, stream)
+
+
+def rdx_max_i32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d int32 tensor: the maximum of an int32 tensor (empty gives -2^31)."""
+    return _scalar("rdx_max_i32", x, (torch.int32,), torch.int32, out, stream)
+
+
 def rdx_rowsum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """(rows,) float32 tensor: per-row sums of a contiguous 2-D float32 tensor."""
     lib = load()
@@ -191,11 +204,12 @@ def rdx_rowsum_strided_f32(x: torch.Tensor, out: torch.Tensor | None = None, str
 
 # RDX_OP_* codes of include/rdx.h, by operation name.
 OP_CODES = {"sum_f32": 0, "sumsq_f32": 1, "sum_bf16": 2, "sumsq_bf16": 3, "sum_i32": 4,
-            "sum_sumsq_f32": 5, "sum_sumsq_bf16": 6}
+            "sum_sumsq_f32": 5, "sum_sumsq_bf16": 6, "max_f32": 7, "max_i32": 8}
 _OP_IN = {0: (torch.float32,), 1: (torch.float32,), 2: _BF16, 3: _BF16, 4: (torch.int32,), 5: (torch.float32,),
-          6: _BF16}
+          6: _BF16, 7: (torch.float32,), 8: (torch.int32,)}
 _OP_OUT = {0: (torch.float32, ()), 1: (torch.float32, ()), 2: (torch.float32, ()), 3: (torch.float32, ()),
-           4: (torch.int64, ()), 5: (torch.float32, (2,)), 6: (torch.float32, (2,))}
+           4: (torch.int64, ()), 5: (torch.float32, (2,)), 6: (torch.float32, (2,)), 7: (torch.float32, ()),
+           8: (torch.int32, ())}
 
 
 def rdx_workspace_bytes() -> int:
@@ -221,6 +235,19 @@ def rdx_reduce_ws(op, x: torch.Tensor, workspace: torch.Tensor, out: torch.Tenso
                                workspace.numel() * workspace.element_size(), _stream_handle(stream, x.device))
     _check("rdx_reduce_ws", st)
     return out
+
+
+def rdx_bank_probe(pattern: int, iters: int = 256, device=None, stream=None) -> float:
+    """Clock cycles per shared-memory load instruction of the page's bank
+    pattern ``pattern`` (0..9), measured by one warp on the GPU."""
+    lib = load()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    cycles = torch.zeros(1, dtype=torch.int64, device=device)
+    sink = torch.zeros(32, dtype=torch.int32, device=device)
+    with torch.cuda.device(device):
+        st = lib.rdx_bank_probe(pattern, iters, cycles.data_ptr(), sink.data_ptr(), _stream_handle(stream, device))
+    _check("rdx_bank_probe", st)
+    return cycles.item() / (iters * lib.rdx_bank_probe_loads_per_iter())
 
 
 def rdx_ladder_num_partials(version: int, n: int) -> int:
@@ -264,6 +291,8 @@ SCALAR_OPS = {
     "sum_bf16": rdx_sum_bf16_f32acc,
     "sumsq_bf16": rdx_sumsq_bf16_f32acc,
     "sum_i32": rdx_sum_i32_i64,
+    "max_f32": rdx_max_f32,
+    "max_i32": rdx_max_i32,
 }
 
 # One-pass [sum, sum of squares] entry points by input type.

@@ -201,6 +201,14 @@ rdx_status rdx_sum_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out2, 
     return reduce_entry(Op::SumSumSqBF16, x, n, out2, stream);
 }
 
+rdx_status rdx_max_f32(const float* x, int64_t n, float* out, cudaStream_t stream) {
+    return reduce_entry(Op::MaxF32, x, n, out, stream);
+}
+
+rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t stream) {
+    return reduce_entry(Op::MaxI32, x, n, out, stream);
+}
+
 size_t rdx_workspace_bytes(void) { return workspace_bytes(); }
 
 rdx_status rdx_reduce_ws(int op, const void* x, int64_t n, void* out, void* workspace, size_t workspace_size,
@@ -252,6 +260,23 @@ rdx_status rdx_ladder_partials_f32(int version, const float* x, int64_t n, float
     if (e != cudaSuccess) return fail_cuda("ladder kernel launch", e);
     return RDX_OK;
 }
+
+rdx_status rdx_bank_probe(int pattern, int iters, int64_t* cycles, uint32_t* sink, cudaStream_t stream) {
+    t_last_error.clear();
+    if (pattern < 0 || pattern >= rdx::kBankPatterns || iters < 1 || iters > (1 << 20)) return RDX_ERR_INVALID_ARG;
+    if (cycles == nullptr || sink == nullptr || !is_aligned(cycles, 8) || !is_aligned(sink, 4))
+        return RDX_ERR_INVALID_ARG;
+    if (overlaps(cycles, 8, sink, 32 * 4)) return RDX_ERR_INVALID_ARG;
+    const DeviceCaps* dev = nullptr;
+    const rdx_status st = current_device(&dev);
+    if (st != RDX_OK) return st;
+    const cudaError_t e = rdx::bank_probe_launch(pattern, iters, reinterpret_cast<long long*>(cycles),
+                                                 reinterpret_cast<unsigned*>(sink), stream);
+    if (e != cudaSuccess) return fail_cuda("bank probe launch", e);
+    return RDX_OK;
+}
+
+int rdx_bank_probe_loads_per_iter(void) { return rdx::bank_probe_loads_per_iter(); }
 
 const char* rdx_status_string(rdx_status status) {
     switch (status) {

@@ -58,6 +58,7 @@ struct SumF32 {
     using In = float;
     using Acc = float;
     static constexpr int kVec = 4;
+    __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return v; }
     __device__ static Acc fold(uint4 v) {
         return (__uint_as_float(v.x) + __uint_as_float(v.y)) + (__uint_as_float(v.z) + __uint_as_float(v.w));
@@ -68,6 +69,7 @@ struct SumSqF32 {
     using In = float;
     using Acc = float;
     static constexpr int kVec = 4;
+    __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return v * v; }
     __device__ static Acc fold(uint4 v) {
         const float a = __uint_as_float(v.x), b = __uint_as_float(v.y);
@@ -80,6 +82,7 @@ struct SumBF16 {
     using In = uint16_t;
     using Acc = float;
     static constexpr int kVec = 8;
+    __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return __uint_as_float(uint32_t(v) << 16); }
     __device__ static float pair(uint32_t w) { return bf16_lo(w) + bf16_hi(w); }
     __device__ static Acc fold(uint4 v) { return (pair(v.x) + pair(v.y)) + (pair(v.z) + pair(v.w)); }
@@ -89,6 +92,7 @@ struct SumSqBF16 {
     using In = uint16_t;
     using Acc = float;
     static constexpr int kVec = 8;
+    __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) {
         const float f = __uint_as_float(uint32_t(v) << 16);
         return f * f;
@@ -107,6 +111,7 @@ struct SumI32 {
     // int64 addition is exact and associative: the grouping cannot change the
     // result, so one accumulator per thread is enough (and saves registers).
     static constexpr bool kExact = true;
+    __device__ static Acc identity() { return 0; }
     __device__ static Acc term(In v) { return Acc(v); }
     __device__ static Acc fold(uint4 v) {
         return (Acc(int32_t(v.x)) + Acc(int32_t(v.y))) + (Acc(int32_t(v.z)) + Acc(int32_t(v.w)));
@@ -133,6 +138,7 @@ struct SumSumSqF32 {
     using In = float;
     using Acc = SumSq2;
     static constexpr int kVec = 4;
+    __device__ static Acc identity() { return Acc(0.f); }
     __device__ static Acc term(In v) { return Acc(SumF32::term(v), SumSqF32::term(v)); }
     __device__ static Acc fold(uint4 v) { return Acc(SumF32::fold(v), SumSqF32::fold(v)); }
 };
@@ -141,8 +147,62 @@ struct SumSumSqBF16 {
     using In = uint16_t;
     using Acc = SumSq2;
     static constexpr int kVec = 8;
+    __device__ static Acc identity() { return Acc(0.f); }
     __device__ static Acc term(In v) { return Acc(SumBF16::term(v), SumSqBF16::term(v)); }
     __device__ static Acc fold(uint4 v) { return Acc(SumBF16::fold(v), SumSqBF16::fold(v)); }
+};
+
+// Maximum.  The page "lecture02/simt.py" models atomic_max as "replace the
+// stored value if the new one is greater"; folded from -Inf that is the
+// maximum, with NaNs never winning.  fmaxf returns the other operand when one
+// is NaN, so the same rule holds here in any grouping: the result does not
+// depend on the order (up to the sign of a zero maximum).  The accumulator's
+// "+" is the maximum, so the sum trees serve unchanged.
+struct MaxAccF {
+    float v;
+    MaxAccF() = default;
+    __host__ __device__ explicit MaxAccF(float x) : v(x) {}
+};
+__device__ __forceinline__ MaxAccF operator+(MaxAccF a, MaxAccF b) { return MaxAccF(fmaxf(a.v, b.v)); }
+__device__ __forceinline__ MaxAccF& operator+=(MaxAccF& a, MaxAccF b) {
+    a.v = fmaxf(a.v, b.v);
+    return a;
+}
+
+struct MaxAccI {
+    int v;
+    MaxAccI() = default;
+    __host__ __device__ explicit MaxAccI(int x) : v(x) {}
+};
+__device__ __forceinline__ MaxAccI operator+(MaxAccI a, MaxAccI b) { return MaxAccI(max(a.v, b.v)); }
+__device__ __forceinline__ MaxAccI& operator+=(MaxAccI& a, MaxAccI b) {
+    a.v = max(a.v, b.v);
+    return a;
+}
+
+struct MaxF32 {
+    using In = float;
+    using Acc = MaxAccF;
+    static constexpr int kVec = 4;
+    static constexpr bool kExact = true;  // max is exact in any grouping
+    __device__ static Acc identity() { return Acc(-__int_as_float(0x7f800000)); }  // -Inf
+    __device__ static Acc term(In v) { return Acc(v); }
+    __device__ static Acc fold(uint4 v) {
+        return Acc(fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                         fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+    }
+};
+
+struct MaxI32 {
+    using In = int32_t;
+    using Acc = MaxAccI;
+    static constexpr int kVec = 4;
+    static constexpr bool kExact = true;
+    __device__ static Acc identity() { return Acc(int(0x80000000u)); }  // -2^31
+    __device__ static Acc term(In v) { return Acc(v); }
+    __device__ static Acc fold(uint4 v) {
+        return Acc(max(max(int(v.x), int(v.y)), max(int(v.z), int(v.w))));
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -154,6 +214,10 @@ __device__ __forceinline__ long long shfl_down(long long v, int off) { return __
 __device__ __forceinline__ SumSq2 shfl_down(SumSq2 v, int off) {
     return SumSq2(shfl_down(v.s, off), shfl_down(v.q, off));
 }
+__device__ __forceinline__ MaxAccF shfl_down(MaxAccF v, int off) { return MaxAccF(shfl_down(v.v, off)); }
+__device__ __forceinline__ MaxAccI shfl_down(MaxAccI v, int off) {
+    return MaxAccI(__shfl_down_sync(kFullMask, v.v, off));
+}
 
 // Loads of values other blocks wrote in this kernel: through L2 (ld.global.cg),
 // never a stale L1 line.
@@ -163,6 +227,10 @@ __device__ __forceinline__ SumSq2 load_cg(const SumSq2* p) {
     const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
     return SumSq2(v.x, v.y);
 }
+__device__ __forceinline__ MaxAccF load_cg(const MaxAccF* p) {
+    return MaxAccF(__ldcg(reinterpret_cast<const float*>(p)));
+}
+__device__ __forceinline__ MaxAccI load_cg(const MaxAccI* p) { return MaxAccI(__ldcg(reinterpret_cast<const int*>(p))); }
 
 // ---------------------------------------------------------------------------
 // Trees.
@@ -205,7 +273,7 @@ __device__ __forceinline__ T fold_array(T (&a)[N]) {
 // not be in use by other threads when called; the call ends before any
 // thread may write smem again only after a later __syncthreads().
 template <int kBlock, class T>
-__device__ __forceinline__ T block_sum(T v, T* smem) {
+__device__ __forceinline__ T block_sum(T v, T* smem, T identity) {
     constexpr int kWarps = kBlock / kWarpSize;
     static_assert(kWarps <= kWarpSize, "block too large for a one-warp second stage");
     v = warp_sum(v);
@@ -213,9 +281,9 @@ __device__ __forceinline__ T block_sum(T v, T* smem) {
     const int warp = threadIdx.x / kWarpSize;
     if (lane == 0) smem[warp] = v;
     __syncthreads();
-    T r = T(0);
+    T r = identity;
     if (warp == 0) {
-        r = lane < kWarps ? smem[lane] : T(0);
+        r = lane < kWarps ? smem[lane] : identity;
         r = warp_sum(r);
     }
     return r;

@@ -8,9 +8,20 @@
 
 namespace rdx {
 
-// The scalar reductions of the C ABI (the last two give sum and sum of squares
-// in one pass).
-enum class Op : int { SumF32 = 0, SumSqF32, SumBF16, SumSqBF16, SumI32, SumSumSqF32, SumSumSqBF16, kCount };
+// The scalar reductions of the C ABI, numbered as the RDX_OP_* codes
+// (SumSumSq*: sum and sum of squares in one pass).
+enum class Op : int {
+    SumF32 = 0,
+    SumSqF32,
+    SumBF16,
+    SumSqBF16,
+    SumI32,
+    SumSumSqF32,
+    SumSumSqBF16,
+    MaxF32,
+    MaxI32,
+    kCount
+};
 
 // Properties of the current device that the launch heuristics need.
 struct DeviceCaps {
@@ -53,6 +64,12 @@ cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, i
 // (few, long rows: each row split over many blocks).
 bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols);
 constexpr int64_t kMaxSplitRows = 2048;
+
+// ---- the page's bank-conflict probe (banks.cu) -------------------------------
+constexpr int kBankPatterns = 10;
+int bank_probe_loads_per_iter();
+// One warp; cycles[0] = clock cycles of iters * loads_per_iter loads; sink: 32 words.
+cudaError_t bank_probe_launch(int pattern, int iters, long long* cycles, unsigned* sink, cudaStream_t stream);
 
 // ---- error text shared by every entry point (api.cu) ------------------------
 // Replace the calling thread's rdx_last_cuda_error() text.

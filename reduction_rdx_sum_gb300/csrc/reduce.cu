@@ -96,7 +96,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     auto kAccOf = [](int u) { return kShared ? 0 : u; };
     Acc acc[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) acc[u] = Acc(0);
+    for (int u = 0; u < kUnroll; ++u) acc[u] = P::identity();
 
     // Fewer than V elements before the first 16-byte boundary and after the
     // last whole vector: the first threads of the row's tile 0 take one each.
@@ -121,7 +121,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
         if (j < t1) acc[kAccOf(u)] += P::fold(ld_stream16(xv + j));
     }
 
-    Acc a = block_sum<kBlock>(fold_array(acc), smem);
+    Acc a = block_sum<kBlock>(fold_array(acc), smem, P::identity());
 
     if (gridDim.x == 1) {
         if (threadIdx.x == 0) out[row] = a;
@@ -142,7 +142,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     constexpr int kFinishUnroll = kFinishLoadBytes / int(sizeof(Acc));
     Acc b[kFinishUnroll];
 #pragma unroll
-    for (int u = 0; u < kFinishUnroll; ++u) b[u] = Acc(0);
+    for (int u = 0; u < kFinishUnroll; ++u) b[u] = P::identity();
     const int g = int(gridDim.x);
     int j = threadIdx.x;
     for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
@@ -156,7 +156,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     for (int u = 0; u < kFinishUnroll; ++u) {
         if (j + u * kBlock < g) b[u] += load_cg(rp + j + u * kBlock);
     }
-    const Acc total = block_sum<kBlock>(fold_array(b), smem);
+    const Acc total = block_sum<kBlock>(fold_array(b), smem, P::identity());
     if (threadIdx.x == 0) {
         out[row] = total;
         *counter = 0u;  // ready for the next call on this stream
@@ -185,7 +185,7 @@ int reduce_vec_elems(Op op) {
         case Op::SumBF16:
         case Op::SumSqBF16:
         case Op::SumSumSqBF16: return 8;
-        default: return 4;
+        default: return 4;  // float and int32 inputs
     }
 }
 
@@ -218,6 +218,8 @@ cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int6
         case Op::SumI32: return RDX_LAUNCH(SumI32);
         case Op::SumSumSqF32: return RDX_LAUNCH(SumSumSqF32);
         case Op::SumSumSqBF16: return RDX_LAUNCH(SumSumSqBF16);
+        case Op::MaxF32: return RDX_LAUNCH(MaxF32);
+        case Op::MaxI32: return RDX_LAUNCH(MaxI32);
         default: return cudaErrorInvalidValue;
     }
 #undef RDX_LAUNCH

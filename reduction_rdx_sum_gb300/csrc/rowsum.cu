@@ -172,7 +172,7 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
         for (int u = 0; u < kCtaUnroll; ++u) {
             if (i + u * kCtaBlock < m) acc[u] += SumF32::fold(ld_stream16(rv + i + u * kCtaBlock));
         }
-        const float a = block_sum<kCtaBlock>(fold_array(acc), smem);
+        const float a = block_sum<kCtaBlock>(fold_array(acc), smem, 0.f);
         if (t == 0) out[r] = a;
         __syncthreads();  // smem is reused by the next row
     }

@@ -20,13 +20,14 @@ import torch
 
 from . import abi, inputs
 
-OPS = ("sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32", "rowsum_f32", "sum_f32_noalloc")
+OPS = ("sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32", "rowsum_f32", "sum_f32_noalloc",
+       "sum_sumsq_f32", "sum_sumsq_bf16", "max_f32", "max_i32", "bank_probe")
 
 
 def make_input(op: str, n: int, rows: int, cols: int, seed: int, dev) -> torch.Tensor:
-    if op in ("sum_bf16", "sumsq_bf16"):
+    if op in ("sum_bf16", "sumsq_bf16", "sum_sumsq_bf16"):
         return torch.from_numpy(inputs.normal_bf16_bits(n, seed).view(np.int16)).to(dev)
-    if op == "sum_i32":
+    if op in ("sum_i32", "max_i32"):
         return torch.from_numpy(inputs.integers_i32(n, seed, -(1 << 20), 1 << 20)).to(dev)
     if op == "rowsum_f32":
         return torch.from_numpy(inputs.uniform_f32(rows * cols, seed, -1.0, 1.0).reshape(rows, cols)).to(dev)
@@ -38,6 +39,8 @@ def entry(op: str):
         return abi.rdx_rowsum_f32
     if op == "sum_f32_noalloc":
         return abi.rdx_sum_f32_noalloc
+    if op in ("sum_sumsq_f32", "sum_sumsq_bf16"):
+        return abi.PAIR_OPS[op.split("_")[-1]]
     return abi.SCALAR_OPS[op]
 
 
@@ -68,6 +71,12 @@ def main(argv=None) -> int:
 
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
+    if args.op == "bank_probe":
+        # the page's demo 1: cycles per shared load for each of its ten patterns
+        for pattern in range(10):
+            c = abi.rdx_bank_probe(pattern, iters=max(1, args.iters), device=dev)
+            print(json.dumps({"op": "bank_probe", "pattern": pattern, "cycles_per_load": round(c, 2)}), flush=True)
+        return 0
     x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
     fn = entry(args.op)
     stream = torch.cuda.current_stream(dev)

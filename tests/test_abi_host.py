@@ -45,7 +45,8 @@ FAKE = 1 << 40
 
 @pytest.mark.parametrize("name,esize,osize", [
     ("rdx_sum_f32", 4, 4), ("rdx_sumsq_f32", 4, 4), ("rdx_sum_bf16_f32acc", 2, 4),
-    ("rdx_sumsq_bf16_f32acc", 2, 4), ("rdx_sum_i32_i64", 4, 8)])
+    ("rdx_sumsq_bf16_f32acc", 2, 4), ("rdx_sum_i32_i64", 4, 8), ("rdx_sum_sumsq_f32", 4, 8),
+    ("rdx_sum_sumsq_bf16_f32acc", 2, 8), ("rdx_max_f32", 4, 4), ("rdx_max_i32", 4, 4)])
 def test_scalar_argument_validation(lib, name, esize, osize):
     fn = getattr(lib, name)
     assert fn(FAKE, -1, FAKE + 4096, None) == INVALID                 # negative n
@@ -102,7 +103,7 @@ def test_workspace_entry_validation(lib):
     wsb = lib.rdx_workspace_bytes()
     assert wsb >= 256 + 8192 * 8 and wsb % 256 == 0
     ws = FAKE + (1 << 30)
-    assert f(7, FAKE, 10, FAKE + 4096, ws, wsb, None) == INVALID            # bad op
+    assert f(9, FAKE, 10, FAKE + 4096, ws, wsb, None) == INVALID            # bad op
     assert f(-1, FAKE, 10, FAKE + 4096, ws, wsb, None) == INVALID
     assert f(0, FAKE, 10, FAKE + 4096, None, wsb, None) == INVALID          # no workspace
     assert f(0, FAKE, 10, FAKE + 4096, ws, wsb - 1, None) == INVALID        # too small
@@ -122,3 +123,18 @@ def test_strided_rowsum_validation(lib):
     assert f(FAKE, 4, 10, 20, FAKE + 4 * 65, None) == INVALID               # out inside the last row
     assert f(FAKE, 1 << 40, 8, 1 << 30, FAKE - 64, None) == INVALID         # span overflows
     assert f(None, 0, 10, 20, None, None) == abi.RDX_OK
+
+
+def test_bank_probe_validation(lib):
+    f = lib.rdx_bank_probe
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(-1, 10, FAKE, FAKE + 4096, None) == INVALID
+    assert f(10, 10, FAKE, FAKE + 4096, None) == INVALID
+    assert f(0, 0, FAKE, FAKE + 4096, None) == INVALID
+    assert f(0, (1 << 20) + 1, FAKE, FAKE + 4096, None) == INVALID
+    assert f(0, 10, None, FAKE + 4096, None) == INVALID
+    assert f(0, 10, FAKE + 4, FAKE + 4096, None) == INVALID          # cycles misaligned
+    assert f(0, 10, FAKE, FAKE + 4, None) == INVALID                  # sink overlaps cycles
+    lib.rdx_bank_probe_loads_per_iter.restype = ctypes.c_int
+    assert lib.rdx_bank_probe_loads_per_iter() >= 1

@@ -8,9 +8,10 @@
 // block that the host adds up.  This kernel keeps version 5's shape and takes
 // its ideas further for a GPU with 152 SMs and HBM3e:
 //   * tiles: the 16-byte-aligned body of the input is cut into equal
-//     contiguous tiles, one block per tile (128 KiB tiles for a 1 GiB input,
-//     at most kMaxTiles tiles); the hardware hands tiles to SMs as they free
-//     up, so a slow SM does not hold back the end of the kernel;
+//     contiguous tiles, one block per tile (8192 tiles of 128 KiB for a 1 GiB
+//     input, about 1024 tiles of up to 64 KiB for 16-512 MiB inputs, tiles of
+//     at least 16 KiB); the hardware hands tiles to SMs as they free up, so a
+//     slow SM does not hold back the end of the kernel;
 //   * add on load: inside its tile each thread keeps kUnroll independent
 //     16-byte loads in flight and folds each vector into its own register
 //     accumulator (version 4's two elements per thread become dozens);
@@ -49,6 +50,8 @@ constexpr int kBlock = RDX_REDUCE_BLOCK;                  // threads per block
 constexpr int kUnroll = RDX_REDUCE_UNROLL;                // 16-byte loads in flight per thread
 constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // tiles (= partials) aimed at per call
 constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per tile, at least
+constexpr int64_t kMidTiles = 1024;                       // tiles aimed at for mid-size inputs
+constexpr int64_t kMidTileCap = 4096;                     // largest tile of the mid-size rule (64 KiB)
 constexpr int kFinishLoadBytes = 32;                      // partial bytes in flight per thread, last block
 // 8 resident blocks of 256 threads fill an SM (2048 threads): at most 32
 // registers per thread, so every dtype streams with full occupancy.
@@ -198,8 +201,16 @@ size_t reduce_acc_bytes(Op op) {
 ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     ReducePlan p;
     const int64_t mmax = cols / reduce_vec_elems(op);  // whole vectors of a row, at most
-    const int64_t target = kMaxTiles / (rows > 0 ? rows : 1);
+    const int64_t r = rows > 0 ? rows : 1;
+    // large inputs: up to kMaxTiles tiles, many waves for the block scheduler
+    const int64_t target = kMaxTiles / r;
     int64_t tile = (mmax + target - 1) / (target > 0 ? target : 1);
+    // mid-size inputs: about kMidTiles tiles of at most kMidTileCap vectors
+    // (fewer, longer blocks: less per-block overhead where the whole input
+    // is only a few waves deep)
+    const int64_t mid = (r * mmax + kMidTiles - 1) / kMidTiles;
+    const int64_t mid_tile = mid < kMidTileCap ? mid : kMidTileCap;
+    if (tile < mid_tile) tile = mid_tile;
     tile = (tile + kBlock - 1) / kBlock * kBlock;  // whole blocks of vectors
     if (tile < kMinTile) tile = kMinTile;
     p.tile = tile;

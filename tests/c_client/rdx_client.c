@@ -1,0 +1,99 @@
+/* A plain C11 client of librdx.so: device memory from the CUDA runtime, no
+ * C++ and no PyTorch.  Checks a few entry points against closed forms
+ * (inputs are small integers, so every float sum is exact). */
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <cuda_runtime_api.h>
+
+#include "rdx.h"
+
+#define CHECK_CUDA(call)                                                         \
+    do {                                                                         \
+        cudaError_t e_ = (call);                                                 \
+        if (e_ != cudaSuccess) {                                                 \
+            fprintf(stderr, "%s: %s\n", #call, cudaGetErrorString(e_));          \
+            return 2;                                                            \
+        }                                                                        \
+    } while (0)
+
+#define CHECK_RDX(call)                                                          \
+    do {                                                                         \
+        rdx_status s_ = (call);                                                  \
+        if (s_ != RDX_OK) {                                                      \
+            fprintf(stderr, "%s: %s %s\n", #call, rdx_status_string(s_),         \
+                    rdx_last_cuda_error());                                      \
+            return 3;                                                            \
+        }                                                                        \
+    } while (0)
+
+int main(void) {
+    const int64_t n = ((int64_t)1 << 22) + 3; /* 4 Mi + 3 elements */
+    const int64_t rows = 1000, cols = 4099;   /* rows*cols < n */
+    float* hf = (float*)malloc((size_t)n * sizeof(float));
+    int32_t* hi = (int32_t*)malloc((size_t)n * sizeof(int32_t));
+    if (!hf || !hi) return 4;
+    for (int64_t i = 0; i < n; ++i) {
+        hf[i] = (float)(i % 7);               /* 0..6 */
+        hi[i] = (int32_t)((i % 2001) - 1000); /* -1000..1000 */
+    }
+    /* closed forms: n = 7q + r gives 21q + r(r-1)/2; the int series repeats every 2001 */
+    const int64_t q = n / 7, r = n % 7;
+    const double sum_f = 21.0 * (double)q + (double)(r * (r - 1) / 2);
+    int64_t sum_i = 0;
+    for (int64_t i = (n / 2001) * 2001; i < n; ++i) sum_i += (i % 2001) - 1000; /* whole periods sum to 0 */
+
+    float *df, *dout, *drows, *dmax;
+    int32_t *di, *dimax;
+    int64_t* dsum_i;
+    void* ws;
+    cudaStream_t s;
+    CHECK_CUDA(cudaStreamCreate(&s));
+    CHECK_CUDA(cudaMalloc((void**)&df, (size_t)n * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&di, (size_t)n * sizeof(int32_t)));
+    CHECK_CUDA(cudaMalloc((void**)&dout, 2 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dmax, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dimax, sizeof(int32_t)));
+    CHECK_CUDA(cudaMalloc((void**)&dsum_i, sizeof(int64_t)));
+    CHECK_CUDA(cudaMalloc((void**)&drows, (size_t)rows * sizeof(float)));
+    CHECK_CUDA(cudaMalloc(&ws, rdx_workspace_bytes()));
+    CHECK_CUDA(cudaMemset(ws, 0, rdx_workspace_bytes()));
+    CHECK_CUDA(cudaMemcpy(df, hf, (size_t)n * sizeof(float), cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(di, hi, (size_t)n * sizeof(int32_t), cudaMemcpyHostToDevice));
+
+    CHECK_RDX(rdx_sum_f32(df, n, dout, s));
+    CHECK_RDX(rdx_sum_i32_i64(di, n, dsum_i, s));
+    CHECK_RDX(rdx_max_f32(df, n, dmax, s));
+    CHECK_RDX(rdx_max_i32(di, n, dimax, s));
+    CHECK_RDX(rdx_rowsum_f32(df, rows, cols, drows, s));
+    float got_f = 0.f, got_max = 0.f, pair[2] = {0.f, 0.f};
+    int32_t got_imax = 0;
+    int64_t got_i = 0;
+    float* got_rows = (float*)malloc((size_t)rows * sizeof(float));
+    CHECK_CUDA(cudaMemcpyAsync(&got_f, dout, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_i, dsum_i, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_max, dmax, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_imax, dimax, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(got_rows, drows, (size_t)rows * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_RDX(rdx_reduce_ws(RDX_OP_SUM_SUMSQ_F32, df, n, dout, ws, rdx_workspace_bytes(), s));
+    CHECK_CUDA(cudaMemcpyAsync(pair, dout, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaStreamSynchronize(s));
+
+    int bad = 0;
+    if ((double)got_f != sum_f) { fprintf(stderr, "sum_f32 %.1f != %.1f\n", got_f, sum_f); bad = 1; }
+    if (got_i != sum_i) { fprintf(stderr, "sum_i32 %lld != %lld\n", (long long)got_i, (long long)sum_i); bad = 1; }
+    if (got_max != 6.f || got_imax != 1000) { fprintf(stderr, "max %g %d\n", got_max, got_imax); bad = 1; }
+    if ((double)pair[0] != sum_f) { fprintf(stderr, "ws pair sum %.1f\n", pair[0]); bad = 1; }
+    for (int64_t row = 0; row < rows && !bad; ++row) {
+        double e = 0.0;
+        for (int64_t j = 0; j < cols; ++j) e += (double)hf[row * cols + j];
+        if ((double)got_rows[row] != e) { fprintf(stderr, "row %lld: %.1f != %.1f\n", (long long)row, got_rows[row], e); bad = 1; }
+    }
+    /* argument errors come back as statuses, nothing is enqueued */
+    if (rdx_sum_f32(df, -1, dout, s) != RDX_ERR_INVALID_ARG) bad = 1;
+    if (rdx_sum_f32(df, n, (float*)(df + 8), s) != RDX_ERR_INVALID_ARG) bad = 1;
+    rdx_shutdown();
+    printf(bad ? "c client FAILED\n" : "c client ok\n");
+    return bad;
+}

@@ -239,6 +239,39 @@ def calibrate_oracle(arrays, budget_s: float):
     return min(1.0, budget_s * rate / step_bytes())
 
 
+def cpu_threads_rate(arrays):
+    """Context figure, not the oracle: the whole step on every host core with
+    numpy (float64 pairwise sums per chunk of 2^22 elements, int64 for ints),
+    one thread per core.  Reported beside the oracle's single-thread rate."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = os.cpu_count() or 1
+    chunk = 1 << 22
+
+    def work(job):
+        a, lo, hi, kind = job
+        seg = a[lo:hi]
+        if kind == "i":
+            return int(seg.sum(dtype=np.int64))
+        if kind == "b":
+            return float((seg.astype(np.uint32) << 16).view(np.float32).sum(dtype=np.float64))
+        return float(seg.sum(dtype=np.float64))
+
+    jobs = []
+    for w in inputs.SUITE:
+        a = arrays[w.name]
+        kind = "i" if w.op == "sum_i32" else ("b" if "bf16" in w.op else "f")
+        for lo in range(0, a.size, chunk):
+            jobs.append((a, lo, min(a.size, lo + chunk), kind))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        list(ex.map(work, jobs))
+    secs = time.perf_counter() - t0
+    return {"value": round(step_bytes() / secs / 1e9, 2), "unit": UNIT, "cores": cores,
+            "kind": "numpy float64/int64 chunk sums on every core (context only; sums, not squares)",
+            "seconds": round(secs, 2)}
+
+
 # ---------------------------------------------------------------------------
 # the reference arm: the CPU oracle, as it stands, on the host cores
 # ---------------------------------------------------------------------------
@@ -398,6 +431,29 @@ def run_gb300(args):
                         "replaces_us": round(per_config[name[:2] + ("_sum_f32" if "f32" in name else "_sum_bf16")]["us"]
                                              + per_config[name[:2] + ("_sumsq_f32" if "f32" in name else "_sumsq_bf16")]
                                              ["us"], 2)}
+    # configs that fit in the L2 (config 1: 4 MiB; config 2: 64 MiB), flushed
+    # as everywhere else and, labelled as such, with the input left L2-resident
+    small = {w.name: torch.from_numpy(inputs.make(w)).to(dev) for w in inputs.SMALL}
+    for w in inputs.SMALL + (inputs.CFG2_SUM_F32,):
+        xk = small[w.name] if w.name in small else dev_arrays[key2]
+        outk = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=dev)
+        fn = abi.SCALAR_OPS[w.op]
+        ms = time_launches(lambda: fn(xk, out=outk, stream=stream), iters)
+        # L2-resident: 32 back-to-back launches on the same input between two
+        # events (one launch alone would also time the host's launch latency)
+        fn(xk, out=outk, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(32):
+            fn(xk, out=outk, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        hot = e0.elapsed_time(e1) / 32
+        extras[w.name + ("" if w.name in small else "_l2")] = {
+            "us": round(ms * 1e3, 2), "GB/s": round(w.bytes_read / (ms * 1e-3) / 1e9, 1),
+            "l2_resident_us": round(hot * 1e3, 2), "l2_resident_GB/s": round(w.bytes_read / (hot * 1e-3) / 1e9, 1)}
+
     key4 = (inputs.CFG4_ROWSUM_WIDE.dist, inputs.CFG4_ROWSUM_WIDE.seed, inputs.CFG4_ROWSUM_WIDE.numel)
     xs = dev_arrays[key4].view(4, -1)                       # 4 rows of 2^26: the split-row path
     rows_out = torch.empty(4, dtype=torch.float32, device=dev)
@@ -505,6 +561,7 @@ def run_gb300(args):
         line["cpu_baseline"] = {
             "value": round(b / s / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {frac:.2%} of every workload of one step ({b / 1e6:.0f} MB), one thread, {s:.1f} s"}
+        line["cpu_threads_context"] = cpu_threads_rate(arrays)
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)

@@ -106,7 +106,7 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
     const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
     const int64_t nunits = (rows + RU - 1) / RU;
-    for (int64_t k = warp; k < nunits; k += nwarps) {
+    for (int64_t k = warp; k < nunits; k += nwarps) {  // one pass unless the grid is capped
         uint4 v[kRowSteps * 4];
         float sc[kRowSteps];
 #pragma unroll
@@ -193,10 +193,11 @@ cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int6
     constexpr int64_t kRU = (kWarpSize / LPR) * kRowSteps;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
     const int64_t nunits = (rows + kRU - 1) / kRU;
+    // one unit per warp: many short blocks that the hardware hands to SMs as
+    // they free up (measured faster than a capped grid looping over units)
+    (void)dev;
     int64_t blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    // four waves of resident blocks; each warp then loops over its units
-    const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
-    if (blocks > cap) blocks = cap;
+    if (blocks > 0x7fffffff) blocks = 0x7fffffff;
     rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
@@ -208,9 +209,8 @@ cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, in
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
     const int64_t nsteps = (rows + kNG - 1) / kNG;
     int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    // four waves of resident blocks; each warp then loops over its steps
-    const int64_t cap = int64_t(dev.sms) * (dev.rowsum_group_bps > 0 ? dev.rowsum_group_bps : 1) * 4;
-    if (blocks > cap) blocks = cap;
+    (void)dev;  // one step per warp, as in launch_fit
+    if (blocks > 0x7fffffff) blocks = 0x7fffffff;
     rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }

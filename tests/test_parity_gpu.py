@@ -362,3 +362,39 @@ def test_overlap_and_bad_tensors_rejected():
     with pytest.raises(ValueError):
         abi.rdx_sum_f32(torch.ones(10, 10, device=DEV).t())
     assert abi.rdx_sum_f32(x).item() == 1000.0
+
+
+def test_host_threads_call_concurrently():
+    # ctypes drops the GIL during a call: several host threads enqueue on
+    # their own streams at once (per-stream workspaces, no shared state)
+    import threading
+
+    hosts = [inputs.normal_f32((1 << 21) + 17 * i, seed=30 + i) for i in range(6)]
+    devs = [torch.from_numpy(h).to(DEV) for h in hosts]
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(DEV)
+            s = torch.cuda.Stream()
+            outs = []
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    outs.append(abi.rdx_sum_f32(devs[i], stream=s))
+                pair = abi.rdx_sum_sumsq_f32(devs[i], stream=s)
+            s.synchronize()
+            results[i] = ([o.item() for o in outs], pair.tolist())
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(hosts))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, h in enumerate(hosts):
+        sums, pair = results[i]
+        assert len(set(sums)) == 1                     # the same bits every time
+        check("sum_f32", h, sums[0])
+        check("sumsq_f32", h, pair[1])

@@ -394,6 +394,7 @@ def run_gb300(args):
         med = float(np.median(launch_ms[:, k]))
         gbs = w.bytes_read / (med * 1e-3) / 1e9
         per_config[w.name] = {"us": round(med * 1e3, 2), "GB/s": round(gbs, 1),
+                              "Gelem/s": round(w.numel / (med * 1e-3) / 1e9, 1),
                               "frac_of_peak": round(gbs / peak, 4), "bytes": w.bytes_read,
                               "ncu_traffic": ncu_traffic(w.name)}
     shares = launch_ms.sum(axis=0) / launch_ms.sum()

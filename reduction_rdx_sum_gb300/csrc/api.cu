@@ -70,8 +70,8 @@ rdx_status current_device(const DeviceCaps** out) {
     return RDX_OK;
 }
 
-// The (device, stream) workspace; allocated and its counters zeroed (in
-// stream order) on first use.
+// The (device, stream) workspace; allocated, its counters zeroed and its
+// partial slots poisoned (in stream order) on first use.
 rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
     const auto key = std::make_pair(dev.ordinal, reinterpret_cast<uintptr_t>(stream));
@@ -93,9 +93,13 @@ rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** o
         return RDX_ERR_ALLOC;
     }
     e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
+    // Poison the partial slots (all-ones bytes: a NaN for float slots): a
+    // partial read before it was written would show up in the result.
+    if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<char*>(p) + kCounterBytes, 0xFF,
+                                              workspace_bytes() - kCounterBytes, stream);
     if (e != cudaSuccess) {
         cudaFree(p);
-        return fail_cuda("cudaMemsetAsync of the completion counters", e);
+        return fail_cuda("cudaMemsetAsync of the workspace", e);
     }
     g_workspaces.emplace(key, p);
     *out = p;

@@ -53,21 +53,21 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "9b518111557c5ac2"
-_ROW_HASH = "16c6def6542202b3"
+_RED_HASH = "296fb724f81914b3"
+_ROW_HASH = "c8cb0a70080bb591"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2158885902, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2160242702, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2158809102, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2157685774, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1079479296, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1079373824, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67462708, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67466516, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079330304, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079337472, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086256128, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085842432, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

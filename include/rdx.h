@@ -268,6 +268,20 @@ rdx_status rdx_bank_probe(int pattern, int iters, int64_t* cycles, uint32_t* sin
 /* Loads one iteration of rdx_bank_probe issues. */
 int rdx_bank_probe_loads_per_iter(void);
 
+/*
+ * Checked build.  A library compiled with -DRDX_DEBUG=1 tests every global
+ * load and store of its kernels against the buffer it belongs to; an access
+ * outside is skipped, never performed, and counted.  (This stands in for a
+ * memory sanitizer: run the workloads through the checked build and require
+ * a count of zero.)
+ * rdx_debug_build: 1 for a checked build, 0 otherwise.
+ * rdx_debug_violations: *count = out-of-range accesses caught since the last
+ * reset (always 0 in a normal build); synchronizes the device first;
+ * reset != 0 clears the count.  RDX_ERR_INVALID_ARG if count is NULL.
+ */
+int rdx_debug_build(void);
+rdx_status rdx_debug_violations(uint64_t* count, int reset);
+
 /* Static text for a status code ("ok", "invalid argument", ...). */
 const char* rdx_status_string(rdx_status status);
 

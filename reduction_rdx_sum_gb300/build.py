@@ -96,4 +96,8 @@ def build(force: bool = False, defines: list[str] | None = None, out: str = LIB,
 
 if __name__ == "__main__":
     args = sys.argv[1:]
-    build(force="--force" in args, defines=[a for a in args if a.startswith("-D")], verbose=True)
+    defines = [a for a in args if a.startswith("-D")]
+    outs = [a.split("=", 1)[1] for a in args if a.startswith("--out=")]
+    if defines and not outs:
+        raise SystemExit("a build with -D defines needs --out=PATH (the in-tree librdx.so is the default build)")
+    build(force="--force" in args, defines=defines, out=outs[0] if outs else LIB, verbose=True)

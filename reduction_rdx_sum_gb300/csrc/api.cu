@@ -10,6 +10,7 @@
 #include <string>
 #include <utility>
 
+#include "device.cuh"  // RDX_DEBUG
 #include "launch.h"
 
 namespace {
@@ -281,6 +282,27 @@ rdx_status rdx_bank_probe(int pattern, int iters, int64_t* cycles, uint32_t* sin
 }
 
 int rdx_bank_probe_loads_per_iter(void) { return rdx::bank_probe_loads_per_iter(); }
+
+int rdx_debug_build(void) { return RDX_DEBUG ? 1 : 0; }
+
+rdx_status rdx_debug_violations(uint64_t* count, int reset) {
+    t_last_error.clear();
+    if (count == nullptr) return RDX_ERR_INVALID_ARG;
+    *count = 0;
+    if (!RDX_DEBUG) return RDX_OK;
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceSynchronize", e);
+    const unsigned long long parts[3] = {rdx::reduce_out_of_range(reset != 0), rdx::rowsum_out_of_range(reset != 0),
+                                         rdx::ladder_out_of_range(reset != 0)};
+    for (unsigned long long v : parts) {
+        if (v == ~0ull) {
+            t_last_error = "cudaMemcpyFromSymbol of a violation counter failed";
+            return RDX_ERR_CUDA;
+        }
+        *count += v;
+    }
+    return RDX_OK;
+}
 
 const char* rdx_status_string(rdx_status status) {
     switch (status) {

@@ -11,6 +11,42 @@ namespace rdx {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kWarpSize = 32;
 
+// ---------------------------------------------------------------------------
+// Checked build (RDX_DEBUG=1): every global load and store of the kernels
+// first asks guard() whether [p, p + bytes) lies inside the buffer it belongs
+// to, [lo, lo + span).  An access outside is counted and skipped (never
+// performed), so the build can run any input without faulting; the host
+// reads the count through rdx_debug_violations().  In a normal build guard()
+// is the constant true and costs nothing.
+// ---------------------------------------------------------------------------
+#ifndef RDX_DEBUG
+#define RDX_DEBUG 0
+#endif
+#if RDX_DEBUG
+static __device__ unsigned long long g_out_of_range;  // one per translation unit
+__device__ __forceinline__ bool guard(const void* p, size_t bytes, const void* lo, size_t span) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(lo);
+    const bool ok = a >= b && a + bytes <= b + span;
+    if (!ok) atomicAdd(&g_out_of_range, 1ull);
+    return ok;
+}
+// Host side: this translation unit's count (optionally reset to 0).
+#define RDX_DEFINE_VIOLATION_COUNTER(fn)                                           \
+    unsigned long long fn(bool reset) {                                           \
+        unsigned long long v = 0;                                                 \
+        if (cudaMemcpyFromSymbol(&v, g_out_of_range, sizeof v) != cudaSuccess) v = ~0ull; \
+        if (reset) {                                                              \
+            const unsigned long long z = 0;                                       \
+            cudaMemcpyToSymbol(g_out_of_range, &z, sizeof z);                     \
+        }                                                                         \
+        return v;                                                                 \
+    }
+#else
+__device__ __forceinline__ constexpr bool guard(const void*, size_t, const void*, size_t) { return true; }
+#define RDX_DEFINE_VIOLATION_COUNTER(fn) \
+    unsigned long long fn(bool) { return 0; }
+#endif
+
 // One 16-byte load on the read-only path.  Every input byte is read once, so
 // the line is not kept in L1 (L1::no_allocate); L2::256B asks the L2 to fetch
 // the whole 256-byte span the warp is about to stream through.  The asm is
@@ -58,6 +94,7 @@ struct SumF32 {
     using In = float;
     using Acc = float;
     static constexpr int kVec = 4;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return v; }
     __device__ static Acc fold(uint4 v) {
@@ -69,6 +106,7 @@ struct SumSqF32 {
     using In = float;
     using Acc = float;
     static constexpr int kVec = 4;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return v * v; }
     __device__ static Acc fold(uint4 v) {
@@ -82,6 +120,7 @@ struct SumBF16 {
     using In = uint16_t;
     using Acc = float;
     static constexpr int kVec = 8;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) { return __uint_as_float(uint32_t(v) << 16); }
     __device__ static float pair(uint32_t w) { return bf16_lo(w) + bf16_hi(w); }
@@ -92,6 +131,7 @@ struct SumSqBF16 {
     using In = uint16_t;
     using Acc = float;
     static constexpr int kVec = 8;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return 0.f; }
     __device__ static Acc term(In v) {
         const float f = __uint_as_float(uint32_t(v) << 16);
@@ -111,6 +151,7 @@ struct SumI32 {
     // int64 addition is exact and associative: the grouping cannot change the
     // result, so one accumulator per thread is enough (and saves registers).
     static constexpr bool kExact = true;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return 0; }
     __device__ static Acc term(In v) { return Acc(v); }
     __device__ static Acc fold(uint4 v) {
@@ -138,6 +179,7 @@ struct SumSumSqF32 {
     using In = float;
     using Acc = SumSq2;
     static constexpr int kVec = 4;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return Acc(0.f); }
     __device__ static Acc term(In v) { return Acc(SumF32::term(v), SumSqF32::term(v)); }
     __device__ static Acc fold(uint4 v) { return Acc(SumF32::fold(v), SumSqF32::fold(v)); }
@@ -147,6 +189,7 @@ struct SumSumSqBF16 {
     using In = uint16_t;
     using Acc = SumSq2;
     static constexpr int kVec = 8;
+    __device__ static uint4 neutral() { return make_uint4(0u, 0u, 0u, 0u); }  // folds to the identity
     __device__ static Acc identity() { return Acc(0.f); }
     __device__ static Acc term(In v) { return Acc(SumBF16::term(v), SumSqBF16::term(v)); }
     __device__ static Acc fold(uint4 v) { return Acc(SumBF16::fold(v), SumSqBF16::fold(v)); }
@@ -185,6 +228,7 @@ struct MaxF32 {
     using Acc = MaxAccF;
     static constexpr int kVec = 4;
     static constexpr bool kExact = true;  // max is exact in any grouping
+    __device__ static uint4 neutral() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
     __device__ static Acc identity() { return Acc(-__int_as_float(0x7f800000)); }  // -Inf
     __device__ static Acc term(In v) { return Acc(v); }
     __device__ static Acc fold(uint4 v) {
@@ -198,6 +242,7 @@ struct MaxI32 {
     using Acc = MaxAccI;
     static constexpr int kVec = 4;
     static constexpr bool kExact = true;
+    __device__ static uint4 neutral() { return make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u); }
     __device__ static Acc identity() { return Acc(int(0x80000000u)); }  // -2^31
     __device__ static Acc term(In v) { return Acc(v); }
     __device__ static Acc fold(uint4 v) {

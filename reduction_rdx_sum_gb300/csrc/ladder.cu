@@ -34,15 +34,17 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
     const int tid = threadIdx.x;
     const int64_t bx = blockIdx.x;
 
+    const size_t span = size_t(n) * 4;
     if (V <= 3) {
         const int64_t i = bx * B + tid;
-        sdata[tid] = i < n ? in[i] : 0.f;
+        sdata[tid] = i < n && guard(in + i, 4, in, span) ? in[i] : 0.f;
     } else {
         const int64_t i = bx * (2 * B) + tid;
-        const float a = i < n ? in[i] : 0.f;
-        const float b = i + B < n ? in[i + B] : 0.f;
+        const float a = i < n && guard(in + i, 4, in, span) ? in[i] : 0.f;
+        const float b = i + B < n && guard(in + i + B, 4, in, span) ? in[i + B] : 0.f;
         sdata[tid] = a + b;
     }
+    const size_t out_span = size_t(gridDim.x) * 4;
     __syncthreads();
 
     if (V == 1) {
@@ -69,14 +71,16 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
         if (tid < kWarpSize) {
             float val = sdata[tid] + sdata[tid + 32];
             for (int off = 16; off > 0; off >>= 1) val += __shfl_down_sync(kFullMask, val, off);
-            if (tid == 0) out[bx] = val;
+            if (tid == 0 && guard(out + bx, 4, out, out_span)) out[bx] = val;
         }
         return;
     }
-    if (tid == 0) out[bx] = sdata[0];
+    if (tid == 0 && guard(out + bx, 4, out, out_span)) out[bx] = sdata[0];
 }
 
 }  // namespace
+
+RDX_DEFINE_VIOLATION_COUNTER(ladder_out_of_range)
 
 cudaError_t ladder_launch(int version, const float* x, int64_t n, float* partials, int64_t blocks,
                           cudaStream_t stream) {

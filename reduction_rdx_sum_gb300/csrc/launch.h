@@ -71,6 +71,11 @@ int bank_probe_loads_per_iter();
 // One warp; cycles[0] = clock cycles of iters * loads_per_iter loads; sink: 32 words.
 cudaError_t bank_probe_launch(int pattern, int iters, long long* cycles, unsigned* sink, cudaStream_t stream);
 
+// ---- checked build (RDX_DEBUG=1): out-of-range accesses caught, per file ------
+unsigned long long reduce_out_of_range(bool reset);
+unsigned long long rowsum_out_of_range(bool reset);
+unsigned long long ladder_out_of_range(bool reset);
+
 // ---- error text shared by every entry point (api.cu) ------------------------
 // Replace the calling thread's rdx_last_cuda_error() text.
 void set_last_error(const char* text);

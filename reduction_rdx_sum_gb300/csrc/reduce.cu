@@ -103,17 +103,21 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
 
     // Fewer than V elements before the first 16-byte boundary and after the
     // last whole vector: the first threads of the row's tile 0 take one each.
+    const size_t span = size_t(cols) * sizeof(typename P::In);  // this row's bytes
     if (blockIdx.x == 0) {
         const int64_t tail0 = head + m * V;
-        if (threadIdx.x < head) acc[0] += P::term(xr[threadIdx.x]);
-        if (threadIdx.x < cols - tail0) acc[kUnroll - 1] += P::term(xr[tail0 + threadIdx.x]);
+        if (threadIdx.x < head && guard(xr + threadIdx.x, sizeof(typename P::In), xr, span))
+            acc[0] += P::term(xr[threadIdx.x]);
+        if (threadIdx.x < cols - tail0 && guard(xr + tail0 + threadIdx.x, sizeof(typename P::In), xr, span))
+            acc[kUnroll - 1] += P::term(xr[tail0 + threadIdx.x]);
     }
 
     int64_t i = t0 + threadIdx.x;
     for (; i + (kUnroll - 1) * kBlock < t1; i += kUnroll * kBlock) {
         uint4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(xv + i + u * kBlock);
+        for (int u = 0; u < kUnroll; ++u)
+            v[u] = guard(xv + i + u * kBlock, 16, xr, span) ? ld_stream16(xv + i + u * kBlock) : P::neutral();
         batch_fence(v);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) acc[kAccOf(u)] += P::fold(v[u]);
@@ -121,20 +125,24 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int64_t j = i + u * kBlock;
-        if (j < t1) acc[kAccOf(u)] += P::fold(ld_stream16(xv + j));
+        if (j < t1 && guard(xv + j, 16, xr, span)) acc[kAccOf(u)] += P::fold(ld_stream16(xv + j));
     }
 
     Acc a = block_sum<kBlock>(fold_array(acc), smem, P::identity());
 
+    const size_t out_span = size_t(gridDim.y) * sizeof(Acc);
     if (gridDim.x == 1) {
-        if (threadIdx.x == 0) out[row] = a;
+        if (threadIdx.x == 0 && guard(out + row, sizeof(Acc), out, out_span)) out[row] = a;
         return;
     }
     Acc* __restrict__ rp = partials + row * int64_t(gridDim.x);
     unsigned* counter = counters + row;
+    const size_t part_span = size_t(gridDim.x) * gridDim.y * sizeof(Acc);
     if (threadIdx.x == 0) {
-        rp[blockIdx.x] = a;
-        last_block = take_ticket(counter) == gridDim.x - 1;
+        if (guard(rp + blockIdx.x, sizeof(Acc), partials, part_span)) rp[blockIdx.x] = a;
+        last_block = guard(counter, sizeof(unsigned), counters, gridDim.y * sizeof(unsigned))
+                         ? take_ticket(counter) == gridDim.x - 1
+                         : 0u;
     }
     __syncthreads();
     if (!last_block) return;
@@ -151,18 +159,21 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
         Acc p[kFinishUnroll];
 #pragma unroll
-        for (int u = 0; u < kFinishUnroll; ++u) p[u] = load_cg(rp + j + u * kBlock);
+        for (int u = 0; u < kFinishUnroll; ++u)
+            p[u] = guard(rp + j + u * kBlock, sizeof(Acc), partials, part_span) ? load_cg(rp + j + u * kBlock)
+                                                                              : P::identity();
 #pragma unroll
         for (int u = 0; u < kFinishUnroll; ++u) b[u] += p[u];
     }
 #pragma unroll
     for (int u = 0; u < kFinishUnroll; ++u) {
-        if (j + u * kBlock < g) b[u] += load_cg(rp + j + u * kBlock);
+        if (j + u * kBlock < g && guard(rp + j + u * kBlock, sizeof(Acc), partials, part_span))
+            b[u] += load_cg(rp + j + u * kBlock);
     }
     const Acc total = block_sum<kBlock>(fold_array(b), smem, P::identity());
     if (threadIdx.x == 0) {
-        out[row] = total;
-        *counter = 0u;  // ready for the next call on this stream
+        if (guard(out + row, sizeof(Acc), out, out_span)) out[row] = total;
+        *counter = 0u;  // ready for the next call on this stream (checked above)
     }
 }
 
@@ -177,6 +188,8 @@ cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, 
 }
 
 }  // namespace
+
+RDX_DEFINE_VIOLATION_COUNTER(reduce_out_of_range)
 
 int reduce_block_threads() { return kBlock; }
 int reduce_unroll() { return kUnroll; }

@@ -48,21 +48,26 @@ __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     // up to 3 scalars before the first and after the last whole vector; a
     // group may have fewer than 3 lanes, so stride by LPR
-    for (int64_t k = l; k < head; k += LPR) acc[0] += __ldg(row + k);
-    for (int64_t k = tail0 + l; k < cols; k += LPR) acc[1] += __ldg(row + k);
+    const size_t span = size_t(cols) * 4;
+    for (int64_t k = l; k < head; k += LPR)
+        if (guard(row + k, 4, row, span)) acc[0] += __ldg(row + k);
+    for (int64_t k = tail0 + l; k < cols; k += LPR)
+        if (guard(row + k, 4, row, span)) acc[1] += __ldg(row + k);
     const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
     int64_t j = l;
     for (; j + 3 * LPR < m; j += 4 * LPR) {
         uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = ld_stream16(rv + j + u * LPR);
+        for (int u = 0; u < 4; ++u)
+            v[u] = guard(rv + j + u * LPR, 16, row, span) ? ld_stream16(rv + j + u * LPR) : SumF32::neutral();
         batch_fence(v);
 #pragma unroll
         for (int u = 0; u < 4; ++u) acc[u] += SumF32::fold(v[u]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        if (j + u * LPR < m) acc[u] += SumF32::fold(ld_stream16(rv + j + u * LPR));
+        if (j + u * LPR < m && guard(rv + j + u * LPR, 16, row, span))
+            acc[u] += SumF32::fold(ld_stream16(rv + j + u * LPR));
     }
     return fold_array(acc);
 }
@@ -86,7 +91,7 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int
         float s = 0.f;
         if (r < rows) s = row_share<LPR>(x + r * ld, cols, l);
         s = group_allreduce<LPR>(s);  // every lane takes part, in range or not
-        if (l == 0 && r < rows) out[r] = s;
+        if (l == 0 && r < rows && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = s;
     }
 }
 
@@ -120,12 +125,16 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
                 const int64_t head = row_head(row, cols);
                 const int64_t m = (cols - head) >> 2;
                 const int64_t tail0 = head + 4 * m;
-                for (int64_t e = l; e < head; e += LPR) sc[q] += __ldg(row + e);
-                for (int64_t e = tail0 + l; e < cols; e += LPR) sc[q] += __ldg(row + e);
+                const size_t span = size_t(cols) * 4;
+                for (int64_t e = l; e < head; e += LPR)
+                    if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
+                for (int64_t e = tail0 + l; e < cols; e += LPR)
+                    if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
                 const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    if (l + u * LPR < m) v[q * 4 + u] = ld_stream16(rv + l + u * LPR);
+                    if (l + u * LPR < m && guard(rv + l + u * LPR, 16, row, span))
+                        v[q * 4 + u] = ld_stream16(rv + l + u * LPR);
                 }
             }
         }
@@ -138,7 +147,7 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
             acc[0] += sc[q];
             float s = group_allreduce<LPR>(fold_array(acc));
             const int64_t r = k * RU + q * NG + grp;
-            if (l == 0 && r < rows) out[r] = s;
+            if (l == 0 && r < rows && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = s;
         }
     }
 }
@@ -156,24 +165,28 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
         float acc[kCtaUnroll];
 #pragma unroll
         for (int u = 0; u < kCtaUnroll; ++u) acc[u] = 0.f;
-        if (t < head) acc[0] += __ldg(row + t);
-        if (t < cols - tail0) acc[kCtaUnroll - 1] += __ldg(row + tail0 + t);
+        const size_t span = size_t(cols) * 4;
+        if (t < head && guard(row + t, 4, row, span)) acc[0] += __ldg(row + t);
+        if (t < cols - tail0 && guard(row + tail0 + t, 4, row, span)) acc[kCtaUnroll - 1] += __ldg(row + tail0 + t);
         const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
         int64_t i = t;
         for (; i + (kCtaUnroll - 1) * kCtaBlock < m; i += kCtaUnroll * kCtaBlock) {
             uint4 v[kCtaUnroll];
 #pragma unroll
-            for (int u = 0; u < kCtaUnroll; ++u) v[u] = ld_stream16(rv + i + u * kCtaBlock);
+            for (int u = 0; u < kCtaUnroll; ++u)
+                v[u] = guard(rv + i + u * kCtaBlock, 16, row, span) ? ld_stream16(rv + i + u * kCtaBlock)
+                                                                    : SumF32::neutral();
             batch_fence(v);
 #pragma unroll
             for (int u = 0; u < kCtaUnroll; ++u) acc[u] += SumF32::fold(v[u]);
         }
 #pragma unroll
         for (int u = 0; u < kCtaUnroll; ++u) {
-            if (i + u * kCtaBlock < m) acc[u] += SumF32::fold(ld_stream16(rv + i + u * kCtaBlock));
+            if (i + u * kCtaBlock < m && guard(rv + i + u * kCtaBlock, 16, row, span))
+                acc[u] += SumF32::fold(ld_stream16(rv + i + u * kCtaBlock));
         }
         const float a = block_sum<kCtaBlock>(fold_array(acc), smem, 0.f);
-        if (t == 0) out[r] = a;
+        if (t == 0 && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = a;
         __syncthreads();  // smem is reused by the next row
     }
 }
@@ -216,6 +229,8 @@ cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, in
 }
 
 }  // namespace
+
+RDX_DEFINE_VIOLATION_COUNTER(rowsum_out_of_range)
 
 cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cta_bps, rowsum_cta_kernel, kCtaBlock, 0);

@@ -138,3 +138,12 @@ def test_bank_probe_validation(lib):
     assert f(0, 10, FAKE, FAKE + 4, None) == INVALID                  # sink overlaps cycles
     lib.rdx_bank_probe_loads_per_iter.restype = ctypes.c_int
     assert lib.rdx_bank_probe_loads_per_iter() >= 1
+
+
+def test_normal_build_is_unchecked(lib):
+    assert lib.rdx_debug_build() == 0
+    f = lib.rdx_debug_violations
+    f.argtypes, f.restype = [ctypes.c_void_p, ctypes.c_int], ctypes.c_int
+    count = ctypes.c_uint64(7)
+    assert f(ctypes.byref(count), 0) == abi.RDX_OK and count.value == 0   # no CUDA call in a normal build
+    assert f(None, 0) == INVALID

@@ -372,9 +372,7 @@ def run_gb300(args):
     torch.cuda.synchronize()
 
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops] for _ in range(args.steps)]
-    clocks_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None
-    with ClockSampler(local, clocks_path) as clk:
+    with ClockSampler(local, os.environ.get("RDX_BENCH_CLOCKS_CSV")) as clk:
         barrier(world)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()

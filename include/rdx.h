@@ -223,8 +223,9 @@ int64_t rdx_ladder_num_partials(int version, int64_t n);
 
 /*
  * rdx_sum_f32_noalloc: *out = sum_{i<n} x[i], like rdx_sum_f32, but the call
- * allocates no device memory.  (The surveyed pages have no counterpart: this
- * entry point exists for callers of this library, not for the method.)
+ * allocates no device memory.  (The paper, the pages this library follows,
+ * has no counterpart: this entry point exists for callers of this library,
+ * not for the method.)
  *
  * For callers that may not cudaMalloc while they run: code inside a framework
  * whose allocator owns all device memory (an allocation behind its back is

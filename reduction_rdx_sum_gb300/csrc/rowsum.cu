@@ -239,10 +239,11 @@ cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps) {
 }
 
 bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols) {
-    // fewer rows than two waves of one-block-per-row, each long enough for
-    // at least four tiles
-    const int64_t wave = int64_t(dev.sms) * (dev.rowsum_cta_bps > 0 ? dev.rowsum_cta_bps : 1);
-    return rows <= kMaxSplitRows && rows < 2 * wave && cols >= 16384;
+    // At most kMaxSplitRows rows (fewer than two waves of one block per row
+    // on a 152-SM GPU), each long enough for at least four tiles.  The rule
+    // uses no device property, so a call sums in the same order on any GPU.
+    (void)dev;
+    return rows <= kMaxSplitRows && cols >= 16384;
 }
 
 cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,

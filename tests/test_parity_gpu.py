@@ -398,3 +398,15 @@ def test_host_threads_call_concurrently():
         assert len(set(sums)) == 1                     # the same bits every time
         check("sum_f32", h, sums[0])
         check("sumsq_f32", h, pair[1])
+
+
+def test_shutdown_frees_and_calls_reallocate():
+    x = torch.from_numpy(inputs.normal_f32((1 << 22) + 3, seed=9)).to(DEV)
+    a = abi.rdx_sum_f32(x).clone()
+    torch.cuda.synchronize()
+    abi.rdx_shutdown()
+    b = abi.rdx_sum_f32(x)                     # a fresh workspace, counters zeroed again
+    c = abi.rdx_rowsum_f32(x[: 4 * 1000000].view(4, -1))
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.isfinite(c).all()

@@ -63,8 +63,6 @@ rdx_status current_device(const DeviceCaps** out) {
                            "." + std::to_string(c.cc_minor) + "; this library is built for sm_103a only";
             return RDX_ERR_UNSUPPORTED_DEVICE;
         }
-        if ((e = rdx::rowsum_blocks_per_sm(&c.rowsum_cta_bps, &c.rowsum_group_bps)) != cudaSuccess)
-            return fail_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e);
         it = g_caps.emplace(dev, c).first;
     }
     *out = &it->second;  // map nodes are never erased: the pointer stays valid
@@ -156,7 +154,7 @@ rdx_status rowsum_entry(const float* x, int64_t rows, int64_t cols, int64_t ld, 
     const DeviceCaps* dev = nullptr;
     rdx_status st = current_device(&dev);
     if (st != RDX_OK) return st;
-    if (rdx::rowsum_use_split(*dev, rows, cols)) {
+    if (rdx::rowsum_use_split(rows, cols)) {
         // few long rows: each row over many blocks (tiles + a per-row finish)
         const rdx::ReducePlan plan = rdx::reduce_plan(Op::SumF32, rows, cols);
         void* ws = nullptr;
@@ -167,7 +165,7 @@ rdx_status rowsum_entry(const float* x, int64_t rows, int64_t cols, int64_t ld, 
         if (e != cudaSuccess) return fail_cuda("split-row kernel launch", e);
         return RDX_OK;
     }
-    const cudaError_t e = rdx::rowsum_launch(*dev, x, rows, cols, ld, out, stream);
+    const cudaError_t e = rdx::rowsum_launch(x, rows, cols, ld, out, stream);
     if (e != cudaSuccess) return fail_cuda("rowsum kernel launch", e);
     return RDX_OK;
 }

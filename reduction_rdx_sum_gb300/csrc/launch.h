@@ -23,14 +23,12 @@ enum class Op : int {
     kCount
 };
 
-// Properties of the current device that the launch heuristics need.
+// Properties of the current device (checked once per device).
 struct DeviceCaps {
     int ordinal = -1;
     int sms = 0;  // streaming multiprocessors
     int cc_major = 0;
     int cc_minor = 0;
-    int rowsum_cta_bps = 0;    // resident blocks per SM of the long-row kernel
-    int rowsum_group_bps = 0;  // resident blocks per SM of the short-row kernel
 };
 
 // ---- tiled reductions (reduce.cu) -----------------------------------------
@@ -56,13 +54,11 @@ cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int6
                           void* partials, unsigned* counters, void* out, cudaStream_t stream);
 
 // ---- row-segmented sum (rowsum.cu) ----------------------------------------
-cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps);
 // Rows of `cols` elements starting every `ld` elements; no workspace.
-cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
-                          cudaStream_t stream);
+cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream);
 // Whether a (rows, cols) matrix is better summed by the tiled reduce kernel
 // (few, long rows: each row split over many blocks).
-bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols);
+bool rowsum_use_split(int64_t rows, int64_t cols);
 constexpr int64_t kMaxSplitRows = 2048;
 
 // ---- the page's bank-conflict probe (banks.cu) -------------------------------

@@ -201,14 +201,12 @@ int lanes_per_row(int64_t cols) {
 }
 
 template <int LPR>
-cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
-                       cudaStream_t stream) {
+cudaError_t launch_fit(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     constexpr int64_t kRU = (kWarpSize / LPR) * kRowSteps;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
     const int64_t nunits = (rows + kRU - 1) / kRU;
     // one unit per warp: many short blocks that the hardware hands to SMs as
     // they free up (measured faster than a capped grid looping over units)
-    (void)dev;
     int64_t blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
     rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
@@ -216,13 +214,12 @@ cudaError_t launch_fit(const DeviceCaps& dev, const float* x, int64_t rows, int6
 }
 
 template <int LPR>
-cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
-                         cudaStream_t stream) {
+cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     constexpr int64_t kNG = kWarpSize / LPR;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
     const int64_t nsteps = (rows + kNG - 1) / kNG;
     int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    (void)dev;  // one step per warp, as in launch_fit
+    // one step per warp, as in launch_fit
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
     rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
@@ -232,34 +229,26 @@ cudaError_t launch_group(const DeviceCaps& dev, const float* x, int64_t rows, in
 
 RDX_DEFINE_VIOLATION_COUNTER(rowsum_out_of_range)
 
-cudaError_t rowsum_blocks_per_sm(int* cta_bps, int* group_bps) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cta_bps, rowsum_cta_kernel, kCtaBlock, 0);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(group_bps, rowsum_fit_kernel<16>, kGroupBlock, 0);
-}
-
-bool rowsum_use_split(const DeviceCaps& dev, int64_t rows, int64_t cols) {
+bool rowsum_use_split(int64_t rows, int64_t cols) {
     // At most kMaxSplitRows rows (fewer than two waves of one block per row
     // on a 152-SM GPU), each long enough for at least four tiles.  The rule
     // uses no device property, so a call sums in the same order on any GPU.
-    (void)dev;
     return rows <= kMaxSplitRows && cols >= 16384;
 }
 
-cudaError_t rowsum_launch(const DeviceCaps& dev, const float* x, int64_t rows, int64_t cols, int64_t ld, float* out,
-                          cudaStream_t stream) {
+cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {
-            case 1: return launch_fit<1>(dev, x, rows, cols, ld, out, stream);
-            case 2: return launch_fit<2>(dev, x, rows, cols, ld, out, stream);
-            case 4: return launch_fit<4>(dev, x, rows, cols, ld, out, stream);
-            case 8: return launch_fit<8>(dev, x, rows, cols, ld, out, stream);
-            case 16: return launch_fit<16>(dev, x, rows, cols, ld, out, stream);
-            default: return launch_fit<32>(dev, x, rows, cols, ld, out, stream);
+            case 1: return launch_fit<1>(x, rows, cols, ld, out, stream);
+            case 2: return launch_fit<2>(x, rows, cols, ld, out, stream);
+            case 4: return launch_fit<4>(x, rows, cols, ld, out, stream);
+            case 8: return launch_fit<8>(x, rows, cols, ld, out, stream);
+            case 16: return launch_fit<16>(x, rows, cols, ld, out, stream);
+            default: return launch_fit<32>(x, rows, cols, ld, out, stream);
         }
     }
-    if (cols <= kGroupRowMaxCols) return launch_group<32>(dev, x, rows, cols, ld, out, stream);
+    if (cols <= kGroupRowMaxCols) return launch_group<32>(x, rows, cols, ld, out, stream);
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
     rowsum_cta_kernel<<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();

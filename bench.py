@@ -54,20 +54,20 @@ FLUSH_BYTES = 512 << 20
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
 _RED_HASH = "296fb724f81914b3"
-_ROW_HASH = "c8cb0a70080bb591"
+_ROW_HASH = "7afe3bf2f1984c1b"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2160242702, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2160379918, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2157685774, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2158940174, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1079373824, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1079259136, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67466516, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67454868, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079337472, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079343616, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085842432, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085874176, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

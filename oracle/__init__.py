@@ -51,12 +51,23 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
-def _load():
+def use_library(path: str | None) -> None:
+    """Load the oracle functions from another build of ``oracle.c`` (the pin
+    tests use this to check that planted mistakes are caught); None returns to
+    the default build."""
+    global _lib
+    with _lock:
+        _lib = None
+    if path is not None:
+        _load(path)
+
+
+def _load(path: str | None = None):
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        lib = ctypes.CDLL(path or build())
         p, i64, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
         for name in ("oracle_sum_f32", "oracle_sumsq_f32", "oracle_abssum_f32",
                      "oracle_sum_bf16", "oracle_sumsq_bf16", "oracle_abssum_bf16"):

@@ -44,9 +44,11 @@ def declared_symbols() -> list[str]:
     return sorted(set(re.findall(r"\b(rdx_[a-z0-9_]+)\s*\(", text)))
 
 
-def load(path: str = LIB) -> ctypes.CDLL:
-    """Open librdx.so (once) and declare the C signatures."""
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Open librdx.so (once) and declare the C signatures.  RDX_LIBRARY may
+    name another build of it (the checked build, for instance)."""
     global _lib
+    path = path or os.environ.get("RDX_LIBRARY") or LIB
     with _lock:
         if _lib is not None:
             return _lib
@@ -68,6 +70,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib.rdx_reduce_ws.restype = i32
         lib.rdx_bank_probe.argtypes, lib.rdx_bank_probe.restype = [i32, i32, vp, vp, vp], i32
         lib.rdx_bank_probe_loads_per_iter.argtypes, lib.rdx_bank_probe_loads_per_iter.restype = [], i32
+        lib.rdx_debug_build.argtypes, lib.rdx_debug_build.restype = [], i32
+        lib.rdx_debug_violations.argtypes, lib.rdx_debug_violations.restype = [vp, i32], i32
         lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
@@ -282,6 +286,18 @@ def rdx_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None, stream
 
 def rdx_shutdown() -> None:
     load().rdx_shutdown()
+
+
+def rdx_debug_build() -> bool:
+    """True when the loaded library is the checked build (RDX_DEBUG=1)."""
+    return bool(load().rdx_debug_build())
+
+
+def rdx_debug_violations(reset: bool = False) -> int:
+    """Out-of-range accesses the checked build caught (0 in a normal build)."""
+    count = ctypes.c_uint64(0)
+    _check("rdx_debug_violations", load().rdx_debug_violations(ctypes.byref(count), int(reset)))
+    return int(count.value)
 
 
 # Entry points by operation name, for the tests and the bench.

@@ -18,3 +18,18 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With RDX_LIBRARY naming the checked build, the run fails if any kernel
+    access fell outside its buffer."""
+    if not os.environ.get("RDX_LIBRARY"):
+        return
+    from reduction_rdx_sum_gb300 import abi
+
+    if abi._lib is None or not abi.rdx_debug_build():
+        return
+    n = abi.rdx_debug_violations()
+    print(f"\nchecked build: {n} out-of-range accesses")
+    if n != 0:
+        session.exitstatus = 1

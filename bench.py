@@ -324,211 +324,233 @@ def config_block():
 # the GB300 arm
 # ---------------------------------------------------------------------------
 
+class Gb300:
+    """Device state shared by the GB300 measurements: the step's inputs on the
+    device, its seven launches, the L2 flush and the launching stream."""
+
+    def __init__(self, local: int):
+        import torch
+
+        from reduction_rdx_sum_gb300 import abi
+        from reduction_rdx_sum_gb300.runop import L2Flush
+
+        self.torch, self.abi = torch, abi
+        self.dev = torch.device("cuda", local)
+        abi.load()
+        self.arrays, self.distinct = suite_arrays()
+        self.dev_arrays = {}
+        for key, host in self.distinct.items():
+            t = torch.from_numpy(host.view(np.int16) if host.dtype == np.uint16 else host)
+            self.dev_arrays[key] = t.to(self.dev)
+        self.ops = []  # (workload, entry point, input, output)
+        for w in inputs.SUITE:
+            x = self.dev_arrays[self.key(w)]
+            if w.op == "rowsum_f32":
+                x = x.view(*w.shape)
+                out = torch.empty(w.shape[0], dtype=torch.float32, device=self.dev)
+                fn = abi.rdx_rowsum_f32
+            else:
+                out = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=self.dev)
+                fn = abi.SCALAR_OPS[w.op]
+            self.ops.append((w, fn, x, out))
+        self.flush = L2Flush(self.dev, FLUSH_BYTES)
+        self.stream = torch.cuda.current_stream(self.dev)
+
+    @staticmethod
+    def key(w):
+        return (w.dist, w.seed, w.numel)
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def step(self, record=None):
+        """One pass of the seven launches, each after an (untimed) L2 flush."""
+        for k, (w, fn, x, out) in enumerate(self.ops):
+            self.flush()
+            if record is not None:
+                record[k][0].record(self.stream)
+            fn(x, out=out, stream=self.stream)
+            if record is not None:
+                record[k][1].record(self.stream)
+
+    def time_launch(self, fn, iters):
+        """Median ms of one flushed launch of fn (two untimed first)."""
+        ts = []
+        for it in range(iters + 2):
+            self.flush()
+            e0, e1 = self.event(), self.event()
+            e0.record(self.stream)
+            fn()
+            e1.record(self.stream)
+            self.torch.cuda.synchronize()
+            if it >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def time_back_to_back(self, fn, launches=32):
+        """ms per launch of fn launched back to back (input left in the L2)."""
+        fn()
+        self.torch.cuda.synchronize()
+        e0, e1 = self.event(), self.event()
+        e0.record(self.stream)
+        for _ in range(launches):
+            fn()
+        e1.record(self.stream)
+        self.torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / launches
+
+
+def figures(ms: float, nbytes: int):
+    return {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes}
+
+
+def measure_extras(g: Gb300, per_config, iters):
+    """Entry points outside the step, timed the same way."""
+    torch, abi, s = g.torch, g.abi, g.stream
+    extras = {}
+    key2, key5 = g.key(inputs.CFG2_SUM_F32), g.key(inputs.CFG5_SUM_BF16)
+    pair = torch.empty(2, dtype=torch.float32, device=g.dev)
+    for name, cfg, key, fn in (("c2_sum_sumsq_f32_one_pass", "c2", key2, abi.rdx_sum_sumsq_f32),
+                               ("c5_sum_sumsq_bf16_one_pass", "c5", key5, abi.rdx_sum_sumsq_bf16_f32acc)):
+        xk = g.dev_arrays[key]
+        ms = g.time_launch(lambda: fn(xk, out=pair, stream=s), iters)
+        kind = "f32" if "f32" in name else "bf16"
+        extras[name] = dict(figures(ms, xk.numel() * xk.element_size()),
+                            replaces_us=round(per_config[f"{cfg}_sum_{kind}"]["us"]
+                                              + per_config[f"{cfg}_sumsq_{kind}"]["us"], 2))
+    # configs that fit in the L2 (config 1: 4 MiB; config 2: 64 MiB): flushed
+    # as everywhere else and, labelled as such, with the input L2-resident
+    # (back-to-back launches: one launch alone would also time the host)
+    small = {w.name: torch.from_numpy(inputs.make(w)).to(g.dev) for w in inputs.SMALL}
+    for w in inputs.SMALL + (inputs.CFG2_SUM_F32,):
+        xk = small[w.name] if w.name in small else g.dev_arrays[key2]
+        outk = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=g.dev)
+        fn = abi.SCALAR_OPS[w.op]
+        ms = g.time_launch(lambda: fn(xk, out=outk, stream=s), iters)
+        hot = g.time_back_to_back(lambda: fn(xk, out=outk, stream=s))
+        extras[w.name + ("" if w.name in small else "_l2")] = {
+            "us": round(ms * 1e3, 2), "GB/s": round(w.bytes_read / (ms * 1e-3) / 1e9, 1),
+            "l2_resident_us": round(hot * 1e3, 2), "l2_resident_GB/s": round(w.bytes_read / (hot * 1e-3) / 1e9, 1)}
+    xs = g.dev_arrays[g.key(inputs.CFG4_ROWSUM_WIDE)].view(4, -1)   # 4 rows of 2^26: the split-row path
+    rows_out = torch.empty(4, dtype=torch.float32, device=g.dev)
+    ms = g.time_launch(lambda: abi.rdx_rowsum_f32(xs, out=rows_out, stream=s), iters)
+    extras["rowsum_4x67108864_split"] = figures(ms, 1 << 30)
+    return extras
+
+
+def measure_ladder(g: Gb300, iters):
+    """The page's five block reductions on the config-2 float32 array."""
+    x2 = g.dev_arrays[g.key(inputs.CFG2_SUM_F32)]
+    ladder = {}
+    for v in range(1, 6):
+        part = g.torch.empty(g.abi.rdx_ladder_num_partials(v, x2.numel()), dtype=g.torch.float32, device=g.dev)
+        ms = g.time_launch(lambda: g.abi.rdx_ladder_partials_f32(v, x2, out=part, stream=g.stream), iters)
+        ladder[f"v{v}"] = {"us": round(ms * 1e3, 2), "GB/s": round(x2.numel() * 4 / (ms * 1e-3) / 1e9, 1)}
+    return ladder
+
+
+def measure_e2e(g: Gb300, per_config, steps, world):
+    """The step from pinned host memory.  Every step copies each distinct input
+    host -> device on a copy stream, runs the seven launches on the compute
+    stream as soon as their input has landed, and copies every result back.
+    Arrays go in order of falling compute time, so the reductions of one
+    array overlap the copy of the next.  A step's copies wait for the
+    previous step's launches (they overwrite the inputs those launches read)."""
+    torch, s = g.torch, g.stream
+    pinned = {}
+    for key, host in g.distinct.items():
+        t = torch.empty(host.size, dtype=g.dev_arrays[key].dtype, pin_memory=True)
+        t.numpy()[:] = host.view(np.int16) if host.dtype == np.uint16 else host
+        pinned[key] = t
+    outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for (_, _, _, o) in g.ops]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(o.numel() * o.element_size() for (_, _, _, o) in g.ops)
+    compute_us = {key: 0.0 for key in g.distinct}
+    for (w, _, _, _) in g.ops:
+        compute_us[g.key(w)] += per_config[w.name]["us"]
+    order = sorted(g.distinct, key=lambda k: -compute_us[k])
+    copy_stream = torch.cuda.Stream(g.dev)
+
+    def e2e_step():
+        copy_stream.wait_stream(s)
+        landed = {}
+        with torch.cuda.stream(copy_stream):
+            for key in order:
+                g.dev_arrays[key].copy_(pinned[key], non_blocking=True)
+                landed[key] = torch.cuda.Event()
+                landed[key].record(copy_stream)
+        for key in order:
+            s.wait_event(landed[key])
+            for (w, fn, x, out) in g.ops:
+                if g.key(w) == key:
+                    fn(x, out=out, stream=s)
+        with torch.cuda.stream(s):
+            for (_, _, _, out), oh in zip(g.ops, outs_host):
+                oh.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ea, eb = g.event(), g.event()
+    ea.record(s)
+    for _ in range(steps):
+        e2e_step()
+    eb.record(s)
+    torch.cuda.synchronize()
+    secs = max_over_ranks(world, ea.elapsed_time(eb) / 1e3)
+    return {"value": round(step_bytes() * steps * world / secs / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_GBps": round(h2d * steps / secs / 1e9, 1)}
+
+
 def run_gb300(args):
     import torch
-
-    from reduction_rdx_sum_gb300 import abi
-    from reduction_rdx_sum_gb300.runop import L2Flush
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device; the library has no CPU path")
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
-    dev = torch.device("cuda", local)
-    abi.load()
     peak, peak_kind = load_peak()
-
-    arrays, distinct = suite_arrays()
-    dev_arrays = {}
-    for key, host in distinct.items():
-        t = torch.from_numpy(host.view(np.int16) if host.dtype == np.uint16 else host)
-        dev_arrays[key] = t.to(dev)
-    ops = []
-    for w in inputs.SUITE:
-        x = dev_arrays[(w.dist, w.seed, w.numel)]
-        if w.op == "rowsum_f32":
-            x = x.view(*w.shape)
-            out = torch.empty(w.shape[0], dtype=torch.float32, device=dev)
-            fn = abi.rdx_rowsum_f32
-        else:
-            out = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=dev)
-            fn = abi.SCALAR_OPS[w.op]
-        ops.append((w, fn, x, out))
-    flush = L2Flush(dev, FLUSH_BYTES)
-    stream = torch.cuda.current_stream(dev)
-
-    def one_step(record):
-        for k, (w, fn, x, out) in enumerate(ops):
-            flush()
-            if record is not None:
-                record[k][0].record(stream)
-            fn(x, out=out, stream=stream)
-            if record is not None:
-                record[k][1].record(stream)
+    g = Gb300(local)
 
     for _ in range(args.warmup):
-        one_step(None)
+        g.step()
     torch.cuda.synchronize()
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops] for _ in range(args.steps)]
+    # the timed steps: each launch between two events on its stream
+    events = [[[g.event(), g.event()] for _ in g.ops] for _ in range(args.steps)]
     with ClockSampler(local, os.environ.get("RDX_BENCH_CLOCKS_CSV")) as clk:
         barrier(world)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for s in range(args.steps):
-            one_step(events[s])
+            g.step(events[s])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         barrier(world)
     launch_ms = np.array([[e[0].elapsed_time(e[1]) for e in step] for step in events])  # (steps, ops)
-    device_s = float(launch_ms.sum()) / 1e3
-    device_s = max_over_ranks(world, device_s)
-    total_bytes = step_bytes() * args.steps * world
-    value = total_bytes / device_s / 1e9
+    device_s = max_over_ranks(world, float(launch_ms.sum()) / 1e3)
+    value = step_bytes() * args.steps * world / device_s / 1e9
 
     per_config = {}
-    for k, (w, _, _, _) in enumerate(ops):
+    for k, (w, _, _, _) in enumerate(g.ops):
         med = float(np.median(launch_ms[:, k]))
         gbs = w.bytes_read / (med * 1e-3) / 1e9
         per_config[w.name] = {"us": round(med * 1e3, 2), "GB/s": round(gbs, 1),
                               "Gelem/s": round(w.numel / (med * 1e-3) / 1e9, 1),
                               "frac_of_peak": round(gbs / peak, 4), "bytes": w.bytes_read,
                               "ncu_traffic": ncu_traffic(w.name)}
+    # roofline of the kernel with the largest share of the step's time
     shares = launch_ms.sum(axis=0) / launch_ms.sum()
     top = int(np.argmax(shares))
-    wtop = ops[top][0]
+    wtop = g.ops[top][0]
     achieved = wtop.bytes_read / (float(launch_ms[:, top].mean()) * 1e-3) / 1e9
-    src_hash = kernel_source_hash()
-    traffic = ncu_traffic(wtop.name)
 
-    # ---- extras: entry points outside the step, timed the same way -----------
-    def time_launches(fn, iters):
-        ts = []
-        for it in range(iters + 2):
-            flush()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            if it >= 2:
-                ts.append(e0.elapsed_time(e1))
-        return float(np.median(ts))
-
-    extras = {}
     iters = max(3, min(args.steps, 10))
-    key2 = (inputs.CFG2_SUM_F32.dist, inputs.CFG2_SUM_F32.seed, inputs.CFG2_SUM_F32.numel)
-    key5 = (inputs.CFG5_SUM_BF16.dist, inputs.CFG5_SUM_BF16.seed, inputs.CFG5_SUM_BF16.numel)
-    pair = torch.empty(2, dtype=torch.float32, device=dev)
-    for name, key, fn in (("c2_sum_sumsq_f32_one_pass", key2, abi.rdx_sum_sumsq_f32),
-                          ("c5_sum_sumsq_bf16_one_pass", key5, abi.rdx_sum_sumsq_bf16_f32acc)):
-        xk = dev_arrays[key]
-        ms = time_launches(lambda: fn(xk, out=pair, stream=stream), iters)
-        nb = xk.numel() * xk.element_size()
-        extras[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1), "bytes": nb,
-                        "replaces_us": round(per_config[name[:2] + ("_sum_f32" if "f32" in name else "_sum_bf16")]["us"]
-                                             + per_config[name[:2] + ("_sumsq_f32" if "f32" in name else "_sumsq_bf16")]
-                                             ["us"], 2)}
-    # configs that fit in the L2 (config 1: 4 MiB; config 2: 64 MiB), flushed
-    # as everywhere else and, labelled as such, with the input left L2-resident
-    small = {w.name: torch.from_numpy(inputs.make(w)).to(dev) for w in inputs.SMALL}
-    for w in inputs.SMALL + (inputs.CFG2_SUM_F32,):
-        xk = small[w.name] if w.name in small else dev_arrays[key2]
-        outk = torch.empty((), dtype=torch.int64 if w.op == "sum_i32" else torch.float32, device=dev)
-        fn = abi.SCALAR_OPS[w.op]
-        ms = time_launches(lambda: fn(xk, out=outk, stream=stream), iters)
-        # L2-resident: 32 back-to-back launches on the same input between two
-        # events (one launch alone would also time the host's launch latency)
-        fn(xk, out=outk, stream=stream)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(32):
-            fn(xk, out=outk, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        hot = e0.elapsed_time(e1) / 32
-        extras[w.name + ("" if w.name in small else "_l2")] = {
-            "us": round(ms * 1e3, 2), "GB/s": round(w.bytes_read / (ms * 1e-3) / 1e9, 1),
-            "l2_resident_us": round(hot * 1e3, 2), "l2_resident_GB/s": round(w.bytes_read / (hot * 1e-3) / 1e9, 1)}
-
-    key4 = (inputs.CFG4_ROWSUM_WIDE.dist, inputs.CFG4_ROWSUM_WIDE.seed, inputs.CFG4_ROWSUM_WIDE.numel)
-    xs = dev_arrays[key4].view(4, -1)                       # 4 rows of 2^26: the split-row path
-    rows_out = torch.empty(4, dtype=torch.float32, device=dev)
-    ms = time_launches(lambda: abi.rdx_rowsum_f32(xs, out=rows_out, stream=stream), iters)
-    extras["rowsum_4x67108864_split"] = {"us": round(ms * 1e3, 2), "GB/s": round((1 << 30) / (ms * 1e-3) / 1e9, 1),
-                                         "bytes": 1 << 30}
-
-    # ---- ladder (the page's five block reductions) on the fp32 array --------
-    ladder = {}
-    x2 = dev_arrays[(inputs.CFG2_SUM_F32.dist, inputs.CFG2_SUM_F32.seed, inputs.CFG2_SUM_F32.numel)]
-    for v in range(1, 6):
-        part = torch.empty(abi.rdx_ladder_num_partials(v, x2.numel()), dtype=torch.float32, device=dev)
-        ts = []
-        for it in range(max(3, min(args.steps, 10)) + 2):
-            flush()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            abi.rdx_ladder_partials_f32(v, x2, out=part, stream=stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            if it >= 2:
-                ts.append(e0.elapsed_time(e1))
-        med = float(np.median(ts))
-        ladder[f"v{v}"] = {"us": round(med * 1e3, 2), "GB/s": round(x2.numel() * 4 / (med * 1e-3) / 1e9, 1)}
-
-    # ---- end to end from pinned host memory ----------------------------------
-    # Every step copies each distinct input host -> device (pinned memory, a
-    # copy stream), runs the seven launches on the compute stream as soon as
-    # their input has landed, and copies every result back.  Arrays go in
-    # order of falling compute time, so the reductions of one array overlap
-    # the copy of the next.  A step's copies wait for the previous step's
-    # launches (they overwrite the inputs those launches read).
-    pinned = {}
-    for key, host in distinct.items():
-        t = torch.empty(host.size, dtype=dev_arrays[key].dtype, pin_memory=True)
-        t.numpy()[:] = host.view(np.int16) if host.dtype == np.uint16 else host
-        pinned[key] = t
-    outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for (_, _, _, o) in ops]
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = sum(o.numel() * o.element_size() for (_, _, _, o) in ops)
-    e2e_steps = max(1, min(args.steps, 20))
-    key_of = lambda w: (w.dist, w.seed, w.numel)
-    compute_us = {key: 0.0 for key in distinct}
-    for (w, _, _, _) in ops:
-        compute_us[key_of(w)] += per_config[w.name]["us"]
-    order = sorted(distinct, key=lambda k: -compute_us[k])
-    copy_stream = torch.cuda.Stream(dev)
-
-    def e2e_step():
-        copy_stream.wait_stream(stream)
-        landed = {}
-        with torch.cuda.stream(copy_stream):
-            for key in order:
-                dev_arrays[key].copy_(pinned[key], non_blocking=True)
-                landed[key] = torch.cuda.Event()
-                landed[key].record(copy_stream)
-        for key in order:
-            stream.wait_event(landed[key])
-            for (w, fn, x, out) in ops:
-                if key_of(w) == key:
-                    fn(x, out=out, stream=stream)
-        with torch.cuda.stream(stream):
-            for (_, _, _, out), oh in zip(ops, outs_host):
-                oh.copy_(out, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ea.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    eb.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(world, ea.elapsed_time(eb) / 1e3)
-    e2e_value = step_bytes() * e2e_steps * world / e2e_s / 1e9
+    extras = measure_extras(g, per_config, iters)
+    ladder = measure_ladder(g, iters)
+    e2e = measure_e2e(g, per_config, max(1, min(args.steps, 20)), world)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -538,29 +560,28 @@ def run_gb300(args):
         "frac_of_peak": round(value / peak, 4),
         "per_config": per_config,
         "roofline": {"bound": "hbm", "kernel": wtop.name, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wtop.name),
                      "algorithmic_bytes_per_launch": wtop.bytes_read, "time_share": round(float(shares[top]), 4),
                      "peak_source": f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "h2d_GBps": round(h2d * e2e_steps / e2e_s / 1e9, 1)},
-        "gpu_launches": len(ops) * args.steps,
+        "e2e": e2e,
+        "gpu_launches": len(g.ops) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
         "ladder_fp32_n2^24+13": ladder,
         "extras": extras,
-        "kernel_source_hash": src_hash,
+        "kernel_source_hash": kernel_source_hash(),
     }
     if rank == 0 and world == 1:
         import oracle
 
         oracle.build()
-        frac = calibrate_oracle(arrays, 12.0)
-        b, s = oracle_pass(arrays, frac)
+        frac = calibrate_oracle(g.arrays, 12.0)
+        b, secs = oracle_pass(g.arrays, frac)
         line["cpu_baseline"] = {
-            "value": round(b / s / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {frac:.2%} of every workload of one step ({b / 1e6:.0f} MB), one thread, {s:.1f} s"}
-        line["cpu_threads_context"] = cpu_threads_rate(arrays)
+            "value": round(b / secs / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {frac:.2%} of every workload of one step ({b / 1e6:.0f} MB), one thread, {secs:.1f} s"}
+        line["cpu_threads_context"] = cpu_threads_rate(g.arrays)
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)

@@ -138,3 +138,23 @@ def test_split_rows_one_gib():
     x[3, ::2] = 3.0
     got = abi.rdx_rowsum_f32(x).tolist()
     assert got == [float(cols), -0.5 * cols, float(cols), 2.0 * cols]
+
+
+@pytest.mark.slow
+def test_row_offsets_past_2_to_the_32():
+    # short rows: 2^25 + 3 rows of 128 columns (more than 2^32 elements, 16 GiB)
+    rows = (1 << 25) + 3
+    x = torch.ones((rows, 128), device=DEV)
+    x[-1] = 2.0
+    got = abi.rdx_rowsum_f32(x)
+    assert torch.all(got[:-1] == 128.0) and got[-1].item() == 256.0
+    del x, got
+    torch.cuda.empty_cache()
+    # the split path: 2 rows of 2^31 + 7 columns (16 GiB), each over many blocks
+    cols = (1 << 31) + 7
+    x = torch.ones((2, cols), device=DEV)
+    x[1] = -0.25
+    got = abi.rdx_rowsum_f32(x).tolist()
+    assert abs(got[0] - cols) <= 1e-6 * cols and abs(got[1] + 0.25 * cols) <= 1e-6 * 0.25 * cols
+    del x
+    torch.cuda.empty_cache()

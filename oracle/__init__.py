@@ -14,6 +14,10 @@ Contents
     row-segmented sum, and the maximum by the page's atomic_max rule.  Page
     "03_shared_memory_sync_reduction.py", demo 3: the expected value of every
     reduction version is the float64 sum of the input.
+``threads.c`` (a second library, with ``oracle.c`` linked in)
+    The multi-core CPU baseline: one contiguous chunk per thread, each run
+    through the single-thread loop above, chunk results added in chunk order.
+    Not a parity reference; pinned against the single-thread oracle.
 ``ladder.py``
     The five block-level reduction versions of that page's demo 3, restated in
     numpy float32 in the page's order of operations, giving each block's
@@ -35,20 +39,29 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "_liboracle.so")
+_THREADS_SRC = os.path.join(_HERE, "threads.c")
+_THREADS_LIB = os.path.join(_HERE, "_liboracle_threads.so")
 _CFLAGS = ["-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math"]
 
 _lock = threading.Lock()
 _lib = None
+_threads_lib = None
+
+
+def _compile(out: str, srcs: list[str], libs: list[str], force: bool) -> str:
+    stale = force or not os.path.exists(out) or any(os.path.getmtime(out) < os.path.getmtime(s) for s in srcs)
+    if stale:
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, *srcs, "-o", tmp, *libs], check=True)
+        os.replace(tmp, out)
+    return out
 
 
 def build(force: bool = False) -> str:
-    """Compile ``oracle.c`` into ``_liboracle.so`` next to it (gcc, no GPU)."""
-    stale = force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
-    if stale:
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
-        os.replace(tmp, _LIB)
-    return _LIB
+    """Compile ``oracle.c`` into ``_liboracle.so`` next to it, and the threaded
+    baseline into ``_liboracle_threads.so`` (gcc, no GPU)."""
+    _compile(_THREADS_LIB, [_THREADS_SRC, _SRC], ["-lm", "-lpthread"], force)
+    return _compile(_LIB, [_SRC], ["-lm"], force)
 
 
 def use_library(path: str | None) -> None:
@@ -81,6 +94,21 @@ def _load(path: str | None = None):
         lib.oracle_max_i32.argtypes, lib.oracle_max_i32.restype = [p, i64], ctypes.c_int32
         _lib = lib
         return lib
+
+
+def _load_threads():
+    global _threads_lib
+    with _lock:
+        if _threads_lib is None:
+            build()
+            lib = ctypes.CDLL(_THREADS_LIB)
+            p, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            lib.oracle_threaded_reduce.argtypes = [c_int, p, i64, c_int, p, p]
+            lib.oracle_threaded_reduce.restype = c_int
+            lib.oracle_threaded_rowsum_f32.argtypes = [p, i64, i64, c_int, p]
+            lib.oracle_threaded_rowsum_f32.restype = c_int
+            _threads_lib = lib
+        return _threads_lib
 
 
 def _flat(x: np.ndarray, dtype) -> np.ndarray:
@@ -175,6 +203,47 @@ def rowabssum_f32(x: np.ndarray) -> np.ndarray:
     rows, cols = a.shape
     out = np.empty(rows, dtype=np.float64)
     _load().oracle_rowabssum_f32(_ptr(a), rows, cols, _ptr(out))
+    return out
+
+
+# ---- the multi-core baseline (threads.c) ------------------------------------
+
+_THREADED_OPS = {"sum_f32": (0, np.float32), "sumsq_f32": (1, np.float32), "sum_bf16": (2, np.uint16),
+                 "sumsq_bf16": (3, np.uint16), "sum_i32": (4, np.int32)}
+
+
+def default_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def threaded(op: str, x: np.ndarray, threads: int | None = None):
+    """``op`` (one of sum_f32, sumsq_f32, sum_bf16, sumsq_bf16, sum_i32) on
+    ``threads`` host threads, one contiguous chunk each; float for the float
+    ops, int for sum_i32."""
+    code, dtype = _THREADED_OPS[op]
+    a = _flat(x, dtype)
+    d, i = ctypes.c_double(0.0), ctypes.c_int64(0)
+    rc = _load_threads().oracle_threaded_reduce(code, _ptr(a), a.size, int(threads or default_threads()),
+                                                ctypes.byref(d), ctypes.byref(i))
+    if rc != 0:
+        raise RuntimeError(f"oracle_threaded_reduce({op}) failed")
+    return int(i.value) if op == "sum_i32" else float(d.value)
+
+
+def threaded_rowsum_f32(x: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """Per-row sums with the rows split over ``threads`` host threads."""
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.float32 or a.ndim != 2:
+        raise TypeError("threaded_rowsum_f32 expects a 2-D float32 array")
+    rows, cols = a.shape
+    out = np.empty(rows, dtype=np.float64)
+    if _load_threads().oracle_threaded_rowsum_f32(_ptr(a), rows, cols, int(threads or default_threads()),
+                                                  _ptr(out)) != 0:
+        raise RuntimeError("oracle_threaded_rowsum_f32 failed")
     return out
 
 

@@ -54,7 +54,7 @@ FLUSH_BYTES = 512 << 20
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
 _RED_HASH = "296fb724f81914b3"
-_ROW_HASH = "7afe3bf2f1984c1b"
+_ROW_HASH = "fd8c945f59b048a7"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
     "c5_sum_bf16": {"bytes_per_launch": 2160379918, "sources": _RED, "source_hash": _RED_HASH,
@@ -65,9 +65,9 @@ NCU_TRAFFIC = {
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
     "c2_sum_f32": {"bytes_per_launch": 67454868, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079343616, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1078754816, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085874176, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085862912, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

@@ -160,12 +160,15 @@ rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t s
  *   rows  >= 0; rows == 0 enqueues nothing
  *   cols  >= 0; cols == 0 writes rows zeros
  *   out   rows float32 values; must not overlap x
- * Short and medium rows are summed by a group of threads each, long rows by
- * a block each, with no workspace.  Few, very long rows (fewer than two
- * waves of blocks, at least 16384 columns, at most 2048 rows) are each cut
- * into tiles over many blocks and finished on the device like the scalar
- * sums; that path uses the (device, stream) workspace.  Either way a row's
- * summation order is fixed by its address and length.
+ * Rows of fewer than 64 columns (contiguous) are staged through shared
+ * memory in tiles of whole rows and summed one row per thread; short and
+ * medium rows are summed by a group of threads each, long rows by a block
+ * each, with no workspace.  Few, very long rows (fewer than two waves of
+ * blocks, at least 16384 columns, at most 2048 rows) are each cut into tiles
+ * over many blocks and finished on the device like the scalar sums; that
+ * path uses the (device, stream) workspace.  Either way a row's summation
+ * order is fixed by the matrix's shape and the alignment of its address,
+ * never by the device or the run.
  * Errors: RDX_ERR_INVALID_ARG for negative sizes, rows*cols overflowing
  * int64, NULL or misaligned pointers, overlap; RDX_ERR_ALLOC if the split
  * path's workspace cannot be allocated.

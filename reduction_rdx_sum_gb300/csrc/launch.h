@@ -59,6 +59,9 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
 // Whether a (rows, cols) matrix is better summed by the tiled reduce kernel
 // (few, long rows: each row split over many blocks).
 bool rowsum_use_split(int64_t rows, int64_t cols);
+// Whether contiguous narrow rows go through shared memory (rowsum_narrow_kernel):
+// depends on cols, ld and the 4/8/16-byte alignment of x.
+bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld);
 constexpr int64_t kMaxSplitRows = 2048;
 
 // ---- the page's bank-conflict probe (banks.cu) -------------------------------

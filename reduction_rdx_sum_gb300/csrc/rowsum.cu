@@ -4,6 +4,9 @@
 // On the page "03_shared_memory_sync_reduction.py", demo 3, every block writes
 // the sum of its own contiguous segment to out[blockIdx]: a segmented sum.
 // Here a segment is a row, and the work per row decides who sums it:
+//   * narrow rows (contiguous, cols < kNarrowMaxCols; see rowsum_use_narrow):
+//     the matrix is read as one flat array, tile by tile, into shared
+//     memory, and each thread sums whole rows from there;
 //   * short rows (cols <= kFitRowMaxCols): a group of LPR lanes per row, each
 //     lane holding at most four 16-byte vectors of the row, so a warp sums
 //     32/LPR consecutive rows per step; the loads of kRowSteps steps are
@@ -13,8 +16,8 @@
 //   * long rows: one block per row, the same add-on-load loop and block tree
 //     as the scalar reduction, a direct store of the row's sum.
 // Rows may start every ld >= cols elements (a leading dimension).  A row's
-// summation order depends only on its address and length, never on the grid,
-// so the result is bitwise reproducible.  No workspace is needed.  (Few, very
+// summation order depends only on the shape and the alignment of x, never on
+// the grid or the device, so the result is bitwise reproducible.  No workspace is needed.  (Few, very
 // long rows go to the tiled kernel of reduce.cu instead; see rowsum_use_split.)
 #include "device.cuh"
 #include "launch.h"
@@ -31,6 +34,9 @@ constexpr int64_t kFitRowMaxCols = 512;  // 4 vectors x 32 lanes x 4 floats
 #define RDX_ROW_STEPS 1
 #endif
 constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight together
+constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
+constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
+constexpr int64_t kNarrowMaxCols = 64;   // narrow rows: fewer columns than this
 
 // Elements of a row before its first 16-byte boundary (rows of a matrix with
 // cols % 4 != 0 start at varying alignments).
@@ -191,6 +197,88 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     }
 }
 
+// Narrow rows of a contiguous matrix (ld == cols).  The matrix is read as
+// one flat array cut into tiles of whole rows, at most kNarrowTile floats
+// each, one tile per block.  The block stages its tile in shared memory
+// (16-byte loads of the flat array, all in flight together; scalars for the
+// few floats before the tile's first 16-byte boundary and after its last),
+// then thread t sums rows t, t + kNarrowBlock, ... of the tile and stores
+// them (consecutive threads, consecutive rows).
+//
+// Rows are read from shared memory VEC floats at a time (VEC = 1, 2 or 4,
+// chosen by the launcher so that every row starts on a VEC-float boundary),
+// so a row's sum is VEC chains of every VEC-th term, added at the end (two
+// chains of alternate terms for VEC = 1).  Rows start every cols words:
+// with VEC = 1 for odd cols, VEC = 2 for cols = 2 (mod 4) and VEC = 4 for
+// cols = 4 (mod 8), a warp's reads meet no bank conflict.  The order depends
+// only on cols and VEC.
+template <int VEC>
+__global__ void __launch_bounds__(kNarrowBlock)
+rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
+                     float* __restrict__ out) {
+    __shared__ __align__(16) float tile[kNarrowTile + 4];
+    const int t = threadIdx.x;
+    const int ci = int(cols);
+    const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
+    const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
+    const int len = nr * ci;                          // floats of this tile, <= kNarrowTile
+    const float* __restrict__ p0 = x + r0 * cols;
+    const size_t span = size_t(rows) * size_t(cols) * 4;
+    int h = int(((16u - (unsigned(reinterpret_cast<uintptr_t>(p0)) & 15u)) & 15u) >> 2);
+    if (h > len) h = len;
+    const int m = (len - h) >> 2;                     // whole 16-byte vectors
+    const int tail0 = h + 4 * m;
+    const int s = -h & 3;                             // tile float i lives at tile[s + i]
+    const uint4* __restrict__ pv = reinterpret_cast<const uint4*>(p0 + h);
+
+    constexpr int kLoads = kNarrowTile / 4 / kNarrowBlock;  // vectors per thread, all in flight
+    uint4 v[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+        const int k = t + u * kNarrowBlock;
+        v[u] = k < m && guard(pv + k, 16, x, span) ? ld_stream16(pv + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    batch_fence(v);
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+        const int k = t + u * kNarrowBlock;
+        if (k < m) *reinterpret_cast<uint4*>(tile + s + h + 4 * k) = v[u];
+    }
+    if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
+    if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
+    __syncthreads();
+
+    for (int q = t; q < nr; q += kNarrowBlock) {
+        const float* row = tile + s + q * ci;
+        float sum;
+        if (VEC == 4) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < ci; j += 4) {
+                const float4 e = *reinterpret_cast<const float4*>(row + j);
+                a.x += e.x; a.y += e.y; a.z += e.z; a.w += e.w;
+            }
+            sum = (a.x + a.y) + (a.z + a.w);
+        } else if (VEC == 2) {
+            float2 a = make_float2(0.f, 0.f);
+            for (int j = 0; j < ci; j += 2) {
+                const float2 e = *reinterpret_cast<const float2*>(row + j);
+                a.x += e.x; a.y += e.y;
+            }
+            sum = a.x + a.y;
+        } else {
+            float a0 = 0.f, a1 = 0.f;
+            int j = 0;
+            for (; j + 1 < ci; j += 2) {
+                a0 += row[j];
+                a1 += row[j + 1];
+            }
+            if (j < ci) a0 += row[j];
+            sum = a0 + a1;
+        }
+        if (guard(out + r0 + q, 4, out, size_t(rows) * 4)) out[r0 + q] = sum;
+    }
+}
+
 // Lanes per row: the fewest (a power of two, at most 32) that leave each lane
 // at most four 16-byte vectors of the row.
 int lanes_per_row(int64_t cols) {
@@ -236,8 +324,44 @@ bool rowsum_use_split(int64_t rows, int64_t cols) {
     return rows <= kMaxSplitRows && cols >= 16384;
 }
 
+// Shared-memory read width of the narrow kernel.  Rows start every cols
+// words after the tile's staging offset s = (4 - h) % 4, h the floats before
+// the tile's first 16-byte boundary.  Every tile starts a whole number of
+// rows (cols floats each) after x, so h, s and every row start are even (or
+// multiples of 4) exactly when cols and x's alignment allow it.
+static int narrow_vec(const float* x, int64_t cols) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(x);
+    if (cols % 4 == 0 && a % 16 == 0) return 4;
+    if (cols % 2 == 0 && a % 8 == 0) return 2;
+    return 1;
+}
+
+bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld) {
+    if (ld != cols || cols <= 0 || cols >= kNarrowMaxCols) return false;
+    // 16-byte aligned rows of 16, 24, ... columns: the short-row kernel reads
+    // them as whole vectors and is faster
+    if (cols % 8 == 0 && cols > 8) return false;
+    // lanes of a warp whose VEC-float reads share banks: gcd(cols/VEC, 32/VEC)
+    const int vec = narrow_vec(x, cols);
+    int64_t a = cols / vec, b = 32 / vec;
+    while (b) { const int64_t r = a % b; a = b; b = r; }
+    // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
+    return a <= 2 || (cols <= 8 && a <= 4);
+}
+
 cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
+    if (rowsum_use_narrow(x, cols, ld)) {
+        const int64_t rpt = kNarrowTile / cols;  // whole rows per tile
+        const int64_t blocks = (rows + rpt - 1) / rpt;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        switch (narrow_vec(x, cols)) {
+            case 4: rowsum_narrow_kernel<4><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+            case 2: rowsum_narrow_kernel<2><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+            default: rowsum_narrow_kernel<1><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+        }
+        return cudaGetLastError();
+    }
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {
             case 1: return launch_fit<1>(x, rows, cols, ld, out, stream);

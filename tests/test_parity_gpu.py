@@ -230,6 +230,55 @@ def test_rowsum_parity(shape, offset):
     assert np.all(np.abs(got - ref) <= tol)
 
 
+NARROW_COLS = list(range(1, 66))
+
+
+@pytest.mark.parametrize("cols", NARROW_COLS)
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_rowsum_narrow_parity(cols, offset):
+    # rows below 64 columns are staged through shared memory in tiles of
+    # 4096 floats; three whole tiles and a ragged fourth, at every 4-byte
+    # misalignment of the base
+    rows = 3 * (4096 // cols) + 5
+    host = inputs.uniform_f32(rows * cols, seed=cols * 4 + offset, lo=-1.0, hi=1.0).reshape(rows, cols)
+    x = to_device(host.reshape(-1), offset).view(rows, cols)
+    got = abi.rdx_rowsum_f32(x).cpu().numpy().astype(np.float64)
+    ref = oracle.rowsum_f32(host)
+    tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+    bad = np.nonzero(~(np.abs(got - ref) <= tol))[0]
+    assert bad.size == 0, (bad[:5], got[bad[:5]], ref[bad[:5]])
+
+
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 8, 12, 31, 63])
+@pytest.mark.parametrize("offset", [0, 1, 2])
+def test_rowsum_narrow_exact_integers(cols, offset):
+    # small integers: every partial sum is exact in float32, so each row sum
+    # must equal the integer sum bit for bit (a misplaced, dropped or doubled
+    # element changes it)
+    rows = 2 * (4096 // cols) + 3
+    vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
+    x = to_device(vals, offset).view(rows, cols)
+    got = abi.rdx_rowsum_f32(x).cpu().numpy()
+    want = vals.reshape(rows, cols).astype(np.int64).sum(axis=1)
+    assert np.array_equal(got.astype(np.int64), want)
+    assert np.array_equal(oracle.rowsum_f32(vals.reshape(rows, cols)), want.astype(np.float64))
+
+
+def test_rowsum_narrow_deterministic_and_matches_strided():
+    for cols in (3, 6, 12, 20, 45):
+        x = torch.rand((20_000, cols), device=DEV) * 2 - 1
+        a = abi.rdx_rowsum_f32(x)
+        for _ in range(3):
+            assert torch.equal(abi.rdx_rowsum_f32(x).view(torch.int32), a.view(torch.int32))
+        # the same rows read through a leading dimension take another kernel
+        wide = torch.zeros((20_000, cols + 5), device=DEV)
+        wide[:, :cols] = x
+        b = abi.rdx_rowsum_strided_f32(wide[:, :cols])
+        host = x.cpu().numpy()
+        tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+        assert np.all(np.abs(b.cpu().numpy().astype(np.float64) - a.cpu().numpy().astype(np.float64)) <= 2 * tol)
+
+
 def test_rowsum_degenerate_shapes():
     out = torch.full((5,), 7.0, device=DEV)
     abi.rdx_rowsum_f32(torch.empty((5, 0), device=DEV), out=out)

@@ -113,6 +113,22 @@ def test_row_sums_stay_in_bounds(lib, shape):
     assert violations(lib) == 0
 
 
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 6, 8, 12, 20, 31, 63])
+def test_narrow_row_sums_stay_in_bounds(lib, cols):
+    # contiguous rows of fewer than 64 columns: tiles of whole rows staged in
+    # shared memory, at every 4-byte misalignment of the base
+    rows = 3 * (4096 // cols) + 5
+    host = inputs.uniform_f32(rows * cols, seed=cols, lo=-1.0, hi=1.0).reshape(rows, cols)
+    for offset in range(4):
+        x = to_device(host.reshape(-1), offset)
+        out = torch.empty(rows, device=DEV)
+        assert lib.rdx_rowsum_strided_f32(x.data_ptr(), rows, cols, cols, out.data_ptr(), stream()) == 0
+        torch.cuda.synchronize()
+        tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+        assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - oracle.rowsum_f32(host)) <= tol)
+    assert violations(lib) == 0
+
+
 def test_ladder_stays_in_bounds(lib):
     for v in range(1, 6):
         for n in (1, 255, 257, 513, (1 << 16) + 77):

@@ -53,21 +53,21 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "296fb724f81914b3"
+_RED_HASH = "a4764b4748afc12c"
 _ROW_HASH = "fd8c945f59b048a7"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2160379918, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2159604750, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2158940174, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2157853710, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1079259136, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1079440384, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67454868, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67178752, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1078754816, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079272960, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085862912, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086198784, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

@@ -39,9 +39,9 @@ struct DeviceCaps {
 struct ReducePlan {
     int64_t tile = 0;
     int64_t tiles = 1;
+    bool large = false;  // the deeper kernel variant (8 loads in flight, 4 blocks per SM)
 };
 int reduce_block_threads();
-int reduce_unroll();
 int64_t reduce_max_partials();
 int reduce_vec_elems(Op op);
 size_t reduce_elem_bytes(Op op);

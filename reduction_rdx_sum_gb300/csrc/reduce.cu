@@ -13,7 +13,8 @@
 //     at least 16 KiB); the hardware hands tiles to SMs as they free up, so a
 //     slow SM does not hold back the end of the kernel;
 //   * add on load: inside its tile each thread keeps kUnroll independent
-//     16-byte loads in flight and folds each vector into its own register
+//     16-byte loads in flight (kUnrollLarge, at half the occupancy, for
+//     inputs of many waves) and folds each vector into its own register
 //     accumulator (version 4's two elements per thread become dozens);
 //   * shuffle trees: a warp tree, then one shared-memory word per warp, then
 //     a warp tree over those words (one barrier per block);
@@ -33,9 +34,6 @@
 #ifndef RDX_REDUCE_BLOCK
 #define RDX_REDUCE_BLOCK 256
 #endif
-#ifndef RDX_REDUCE_UNROLL
-#define RDX_REDUCE_UNROLL 4
-#endif
 #ifndef RDX_REDUCE_MAX_TILES
 #define RDX_REDUCE_MAX_TILES 8192
 #endif
@@ -47,7 +45,8 @@ namespace rdx {
 namespace {
 
 constexpr int kBlock = RDX_REDUCE_BLOCK;                  // threads per block
-constexpr int kUnroll = RDX_REDUCE_UNROLL;                // 16-byte loads in flight per thread
+constexpr int kUnroll = 4;                                // 16-byte loads in flight per thread
+constexpr int kUnrollLarge = 8;                           // the same, inputs of kLargeTiles tiles or more
 constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // tiles (= partials) aimed at per call
 constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per tile, at least
 constexpr int64_t kMidTiles = 1024;                       // tiles aimed at for mid-size inputs
@@ -56,7 +55,14 @@ constexpr int kFinishLoadBytes = 32;                      // partial bytes in fl
 // 8 resident blocks of 256 threads fill an SM (2048 threads): at most 32
 // registers per thread, so every dtype streams with full occupancy.
 constexpr int kMinBlocksPerSm = 2048 / kBlock;
-static_assert((kUnroll & (kUnroll - 1)) == 0, "kUnroll must be a power of two");
+// Large inputs (many waves of tiles) stream faster from fewer, deeper
+// blocks: 4 blocks per SM with 8 loads in flight per thread keep the same
+// bytes in flight over half as many concurrent streams (measured: 1.0-1.5 %
+// less time at 1-2 GiB, and slower below 256 MiB, where tiles are short).
+constexpr int kMinBlocksLarge = 4;
+constexpr int64_t kLargeTiles = 4096;
+static_assert((kUnroll & (kUnroll - 1)) == 0 && (kUnrollLarge & (kUnrollLarge - 1)) == 0,
+              "load batches are powers of two");
 static_assert(kMinTile % kBlock == 0, "tiles are whole multiples of the block");
 
 // Completion counter: acquire-release at GPU scope, so the partial this
@@ -71,8 +77,8 @@ __device__ __forceinline__ unsigned take_ticket(unsigned* counter) {
     return old;
 }
 
-template <class P>
-__global__ void __launch_bounds__(kBlock, kMinBlocksPerSm)
+template <class P, int U, int kMinBlocks>
+__global__ void __launch_bounds__(kBlock, kMinBlocks)
 reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, int64_t tile,
               typename P::Acc* __restrict__ partials, unsigned* __restrict__ counters,
               typename P::Acc* __restrict__ out) {
@@ -97,9 +103,9 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     // exact (integer) sums
     constexpr bool kShared = is_exact<P>::value;
     auto kAccOf = [](int u) { return kShared ? 0 : u; };
-    Acc acc[kUnroll];
+    Acc acc[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) acc[u] = P::identity();
+    for (int u = 0; u < U; ++u) acc[u] = P::identity();
 
     // Fewer than V elements before the first 16-byte boundary and after the
     // last whole vector: the first threads of the row's tile 0 take one each.
@@ -109,21 +115,21 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
         if (threadIdx.x < head && guard(xr + threadIdx.x, sizeof(typename P::In), xr, span))
             acc[0] += P::term(xr[threadIdx.x]);
         if (threadIdx.x < cols - tail0 && guard(xr + tail0 + threadIdx.x, sizeof(typename P::In), xr, span))
-            acc[kUnroll - 1] += P::term(xr[tail0 + threadIdx.x]);
+            acc[U - 1] += P::term(xr[tail0 + threadIdx.x]);
     }
 
     int64_t i = t0 + threadIdx.x;
-    for (; i + (kUnroll - 1) * kBlock < t1; i += kUnroll * kBlock) {
-        uint4 v[kUnroll];
+    for (; i + (U - 1) * kBlock < t1; i += U * kBlock) {
+        uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < U; ++u)
             v[u] = guard(xv + i + u * kBlock, 16, xr, span) ? ld_stream16(xv + i + u * kBlock) : P::neutral();
         batch_fence(v);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) acc[kAccOf(u)] += P::fold(v[u]);
+        for (int u = 0; u < U; ++u) acc[kAccOf(u)] += P::fold(v[u]);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t j = i + u * kBlock;
         if (j < t1 && guard(xv + j, 16, xr, span)) acc[kAccOf(u)] += P::fold(ld_stream16(xv + j));
     }
@@ -181,9 +187,15 @@ template <class P>
 cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
                          void* partials, unsigned* counters, void* out, cudaStream_t stream) {
     const dim3 grid(unsigned(plan.tiles), unsigned(rows));
-    reduce_kernel<P><<<grid, kBlock, 0, stream>>>(static_cast<const typename P::In*>(x), cols, ld, plan.tile,
-                                                  static_cast<typename P::Acc*>(partials), counters,
-                                                  static_cast<typename P::Acc*>(out));
+    const auto* xt = static_cast<const typename P::In*>(x);
+    auto* pt = static_cast<typename P::Acc*>(partials);
+    auto* ot = static_cast<typename P::Acc*>(out);
+    if (plan.large)
+        reduce_kernel<P, kUnrollLarge, kMinBlocksLarge><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
+                                                                                     counters, ot);
+    else
+        reduce_kernel<P, kUnroll, kMinBlocksPerSm><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
+                                                                                counters, ot);
     return cudaGetLastError();
 }
 
@@ -192,7 +204,6 @@ cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, 
 RDX_DEFINE_VIOLATION_COUNTER(reduce_out_of_range)
 
 int reduce_block_threads() { return kBlock; }
-int reduce_unroll() { return kUnroll; }
 // rows * tiles <= kMaxTiles for any rows <= kMaxTiles (see reduce_plan)
 int64_t reduce_max_partials() { return kMaxTiles; }
 
@@ -228,6 +239,8 @@ ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     if (tile < kMinTile) tile = kMinTile;
     p.tile = tile;
     p.tiles = mmax > 0 ? (mmax + tile - 1) / tile : 1;
+    // many waves of tiles long enough for whole batches of the deeper kernel
+    p.large = r * p.tiles >= kLargeTiles && tile >= kUnrollLarge * kBlock;
     return p;
 }
 

@@ -95,6 +95,25 @@ def test_scalar_parity_misaligned_base(op, n):
         check(op, host, got)
 
 
+# Inputs of 4096 tiles or more (about 256 MiB) take the deeper kernel variant
+# (8 loads in flight per thread, 4 blocks per SM).  4095 * 4096 whole 16-byte
+# vectors is the last size on the shallow side; one more vector crosses over.
+EDGE_VECTORS = 4095 * 4096
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("extra", [0, 1, 3])
+def test_scalar_parity_across_the_deep_variant_threshold(op, extra):
+    per_vec = VEC[op]
+    n = EDGE_VECTORS * per_vec + extra * per_vec + (extra % 2) * (per_vec - 1)  # ragged tail when extra is odd
+    host = host_input(op, n, seed=extra + 11)
+    for offset in (0, 1):
+        x = to_device(host, offset)
+        a = abi.SCALAR_OPS[op](x).item()
+        check(op, host, a)
+        assert abi.SCALAR_OPS[op](x).item() == a  # bitwise reproducible
+
+
 def test_empty_input_writes_zero():
     for op in OPS:
         dt = {"sum_f32": torch.float32, "sumsq_f32": torch.float32, "sum_bf16": torch.bfloat16,

@@ -14,7 +14,8 @@
 //   * medium rows (cols <= kGroupRowMaxCols): a warp per row, looping over
 //     the row four vectors per lane at a time;
 //   * long rows: one block per row, the same add-on-load loop and block tree
-//     as the scalar reduction, a direct store of the row's sum.
+//     as the scalar reduction (twice the loads in flight at half the
+//     occupancy from kCtaDeepCols columns), a direct store of the row's sum.
 // Rows may start every ld >= cols elements (a leading dimension).  A row's
 // summation order depends only on the shape and the alignment of x, never on
 // the grid or the device, so the result is bitwise reproducible.  No workspace is needed.  (Few, very
@@ -27,8 +28,10 @@ namespace {
 
 constexpr int kCtaBlock = 256;   // threads per row, long rows
 constexpr int kCtaUnroll = 4;    // 16-byte loads in flight per thread, long rows
+constexpr int kCtaUnrollDeep = 8;   // the same for rows of kCtaDeepCols or more, at 4 blocks per SM
+constexpr int64_t kCtaDeepCols = 16384;  // measured: deeper is 1 % faster from here, slower below
 constexpr int kGroupBlock = 256; // threads per block, short rows
-constexpr int64_t kGroupRowMaxCols = 4096;
+constexpr int64_t kGroupRowMaxCols = 5120;  // measured: a block per row is faster from about 6144
 constexpr int64_t kFitRowMaxCols = 512;  // 4 vectors x 32 lanes x 4 floats
 #ifndef RDX_ROW_STEPS
 #define RDX_ROW_STEPS 1
@@ -158,8 +161,12 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     }
 }
 
-// Long rows: one block per row (a block loops over rows r, r + gridDim.x, ...).
-__global__ void __launch_bounds__(kCtaBlock)
+// Long rows: one block per row (a block loops over rows r, r + gridDim.x, ...),
+// U loads of 16 bytes in flight per thread.  Very long rows stream faster with
+// U = 8 at 4 blocks per SM than with U = 4 at 8: the same bytes in flight over
+// half as many concurrent streams.
+template <int U, int kMinBlocks>
+__global__ void __launch_bounds__(kCtaBlock, kMinBlocks)
 rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, float* __restrict__ out) {
     __shared__ float smem[kCtaBlock / kWarpSize];
     const int t = threadIdx.x;
@@ -168,26 +175,26 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
         const int64_t head = row_head(row, cols);
         const int64_t m = (cols - head) >> 2;
         const int64_t tail0 = head + 4 * m;
-        float acc[kCtaUnroll];
+        float acc[U];
 #pragma unroll
-        for (int u = 0; u < kCtaUnroll; ++u) acc[u] = 0.f;
+        for (int u = 0; u < U; ++u) acc[u] = 0.f;
         const size_t span = size_t(cols) * 4;
         if (t < head && guard(row + t, 4, row, span)) acc[0] += __ldg(row + t);
-        if (t < cols - tail0 && guard(row + tail0 + t, 4, row, span)) acc[kCtaUnroll - 1] += __ldg(row + tail0 + t);
+        if (t < cols - tail0 && guard(row + tail0 + t, 4, row, span)) acc[U - 1] += __ldg(row + tail0 + t);
         const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
         int64_t i = t;
-        for (; i + (kCtaUnroll - 1) * kCtaBlock < m; i += kCtaUnroll * kCtaBlock) {
-            uint4 v[kCtaUnroll];
+        for (; i + (U - 1) * kCtaBlock < m; i += U * kCtaBlock) {
+            uint4 v[U];
 #pragma unroll
-            for (int u = 0; u < kCtaUnroll; ++u)
+            for (int u = 0; u < U; ++u)
                 v[u] = guard(rv + i + u * kCtaBlock, 16, row, span) ? ld_stream16(rv + i + u * kCtaBlock)
                                                                     : SumF32::neutral();
             batch_fence(v);
 #pragma unroll
-            for (int u = 0; u < kCtaUnroll; ++u) acc[u] += SumF32::fold(v[u]);
+            for (int u = 0; u < U; ++u) acc[u] += SumF32::fold(v[u]);
         }
 #pragma unroll
-        for (int u = 0; u < kCtaUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             if (i + u * kCtaBlock < m && guard(rv + i + u * kCtaBlock, 16, row, span))
                 acc[u] += SumF32::fold(ld_stream16(rv + i + u * kCtaBlock));
         }
@@ -374,7 +381,10 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
     }
     if (cols <= kGroupRowMaxCols) return launch_group<32>(x, rows, cols, ld, out, stream);
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
-    rowsum_cta_kernel<<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
+    if (cols >= kCtaDeepCols)
+        rowsum_cta_kernel<kCtaUnrollDeep, 4><<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
+    else
+        rowsum_cta_kernel<kCtaUnroll, 8><<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
 

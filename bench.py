@@ -29,6 +29,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -53,8 +54,8 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "a4764b4748afc12c"
-_ROW_HASH = "a05c544e4fe88fec"
+_RED_HASH = "b87e31c269a2af2a"
+_ROW_HASH = "4c8a07d4bdb7556a"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
     "c5_sum_bf16": {"bytes_per_launch": 2159604750, "sources": _RED, "source_hash": _RED_HASH,
@@ -72,14 +73,23 @@ NCU_TRAFFIC = {
 }
 
 
+def code_tokens(text: str) -> str:
+    """C++ source with comments removed and whitespace collapsed: what the
+    compiler sees, so that editing a comment does not read as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(files=None) -> str:
-    """Hash of the kernel sources (all of csrc/, or the named files)."""
+    """Hash of the kernel sources' code (all of csrc/, or the named files),
+    comments and layout excluded."""
     csrc = os.path.join(ROOT, "reduction_rdx_sum_gb300", "csrc")
     names = sorted(files) if files else sorted(os.listdir(csrc))
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

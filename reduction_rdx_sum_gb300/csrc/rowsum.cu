@@ -18,8 +18,9 @@
 //     occupancy from kCtaDeepCols columns), a direct store of the row's sum.
 // Rows may start every ld >= cols elements (a leading dimension).  A row's
 // summation order depends only on the shape and the alignment of x, never on
-// the grid or the device, so the result is bitwise reproducible.  No workspace is needed.  (Few, very
-// long rows go to the tiled kernel of reduce.cu instead; see rowsum_use_split.)
+// the grid or the device, so the result is bitwise reproducible.  No
+// workspace is needed.  (Few, very long rows go to the tiled kernel of
+// reduce.cu instead; see rowsum_use_split.)
 #include "device.cuh"
 #include "launch.h"
 
@@ -217,8 +218,10 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 // so a row's sum is VEC chains of every VEC-th term, added at the end (two
 // chains of alternate terms for VEC = 1).  Rows start every cols words:
 // with VEC = 1 for odd cols, VEC = 2 for cols = 2 (mod 4) and VEC = 4 for
-// cols = 4 (mod 8), a warp's reads meet no bank conflict.  The order depends
-// only on cols and VEC.
+// cols = 4 (mod 8), a warp's reads meet no bank conflict; the launcher
+// (rowsum_use_narrow) takes this kernel only where they share a bank at most
+// 2 ways (4 ways for 8 columns or fewer).  The order depends only on cols and
+// VEC.
 template <int VEC>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,

@@ -575,10 +575,14 @@ def run_gb300(args):
 
         oracle.build()
         frac = calibrate_oracle(g.arrays, 12.0)
-        b, secs = oracle_pass(g.arrays, frac)
+        b, secs, passes = 0, 0.0, 0
+        while passes == 0 or (frac >= 1.0 and secs < 10.0 and passes < 4):  # about 10-30 s of oracle work
+            pb, ps = oracle_pass(g.arrays, frac)
+            b, secs, passes = b + pb, secs + ps, passes + 1
         line["cpu_baseline"] = {
             "value": round(b / secs / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {frac:.2%} of every workload of one step ({b / 1e6:.0f} MB), one thread, {secs:.1f} s"}
+            "sample": f"first {frac:.2%} of every workload of one step, {passes} pass(es) ({b / 1e6:.0f} MB), "
+                      f"one thread, {secs:.1f} s"}
         line["cpu_threads"] = cpu_threads_rate(g.arrays)
     if rank == 0:
         print(json.dumps(line), flush=True)

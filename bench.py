@@ -433,6 +433,16 @@ def measure_extras(g: Gb300, per_config, iters):
     rows_out = torch.empty(4, dtype=torch.float32, device=g.dev)
     ms = g.time_launch(lambda: abi.rdx_rowsum_f32(xs, out=rows_out, stream=s), iters)
     extras["rowsum_4x67108864_split"] = figures(ms, 1 << 30)
+    # narrow rows through shared memory: the same 1 GiB viewed as 3 and 12
+    # columns (algorithmic bytes: 4 per element read and 4 per row written)
+    flat = g.dev_arrays[g.key(inputs.CFG4_ROWSUM_WIDE)].view(-1)
+    for cols in (3, 12):
+        rows = flat.numel() // cols
+        xn = flat[: rows * cols].view(rows, cols)
+        on = torch.empty(rows, dtype=torch.float32, device=g.dev)
+        ms = g.time_launch(lambda: abi.rdx_rowsum_f32(xn, out=on, stream=s), iters)
+        extras[f"rowsum_{rows}x{cols}_narrow"] = dict(figures(ms, rows * cols * 4),
+                                                      read_write_GBps=round(rows * (cols + 1) * 4 / (ms * 1e-3) / 1e9, 1))
     return extras
 
 

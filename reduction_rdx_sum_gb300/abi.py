@@ -91,10 +91,22 @@ def _check(fn: str, status: int) -> None:
         raise RdxError(fn, status, load().rdx_last_cuda_error().decode())
 
 
-def _stream_handle(stream, device) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return int(stream.cuda_stream)
+try:  # the current stream's cudaStream_t by device index, without building a Stream object
+    _current_raw_stream = torch._C._cuda_getCurrentRawStream
+except AttributeError:  # pragma: no cover - builds without the accessor
+    def _current_raw_stream(index: int) -> int:
+        return int(torch.cuda.current_stream(index).cuda_stream)
+
+
+def _launch(fn, device, stream, *args) -> int:
+    """fn(*args, stream handle) with `device` current: the C entry points
+    launch on the current device, in `stream` (default: the current stream
+    of `device`).  The device is switched only when it is not current."""
+    index = device.index if isinstance(device, torch.device) else int(device)
+    if index == torch.cuda.current_device():
+        return fn(*args, _current_raw_stream(index) if stream is None else int(stream.cuda_stream))
+    with torch.cuda.device(index):
+        return fn(*args, _current_raw_stream(index) if stream is None else int(stream.cuda_stream))
 
 
 def _input(x: torch.Tensor, dtypes, what: str) -> torch.Tensor:
@@ -119,8 +131,7 @@ def _scalar(name: str, x: torch.Tensor, dtypes, out_dtype, out, stream, shape=()
     lib = load()
     x = _input(x, dtypes, name)
     out = _output(out, x, out_dtype, shape)
-    with torch.cuda.device(x.device):
-        st = getattr(lib, name)(x.data_ptr(), x.numel(), out.data_ptr(), _stream_handle(stream, x.device))
+    st = _launch(getattr(lib, name), x.device, stream, x.data_ptr(), x.numel(), out.data_ptr())
     _check(name, st)
     return out
 
@@ -181,8 +192,7 @@ def rdx_rowsum_f32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None
         raise ValueError("rdx_rowsum_f32: expected a 2-D tensor")
     rows, cols = x.shape
     out = _output(out, x, torch.float32, (rows,))
-    with torch.cuda.device(x.device):
-        st = lib.rdx_rowsum_f32(x.data_ptr(), rows, cols, out.data_ptr(), _stream_handle(stream, x.device))
+    st = _launch(lib.rdx_rowsum_f32, x.device, stream, x.data_ptr(), rows, cols, out.data_ptr())
     _check("rdx_rowsum_f32", st)
     return out
 
@@ -199,9 +209,7 @@ def rdx_rowsum_strided_f32(x: torch.Tensor, out: torch.Tensor | None = None, str
         raise ValueError("rdx_rowsum_strided_f32: rows must be contiguous (stride(1) == 1)")
     ld = x.stride(0) if rows > 1 else cols
     out = _output(out, x, torch.float32, (rows,))
-    with torch.cuda.device(x.device):
-        st = lib.rdx_rowsum_strided_f32(x.data_ptr(), rows, cols, ld, out.data_ptr(),
-                                        _stream_handle(stream, x.device))
+    st = _launch(lib.rdx_rowsum_strided_f32, x.device, stream, x.data_ptr(), rows, cols, ld, out.data_ptr())
     _check("rdx_rowsum_strided_f32", st)
     return out
 
@@ -234,9 +242,8 @@ def rdx_reduce_ws(op, x: torch.Tensor, workspace: torch.Tensor, out: torch.Tenso
     out = _output(out, x, dt, shape)
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("rdx_reduce_ws: workspace must be a contiguous CUDA tensor")
-    with torch.cuda.device(x.device):
-        st = lib.rdx_reduce_ws(code, x.data_ptr(), x.numel(), out.data_ptr(), workspace.data_ptr(),
-                               workspace.numel() * workspace.element_size(), _stream_handle(stream, x.device))
+    st = _launch(lib.rdx_reduce_ws, x.device, stream, code, x.data_ptr(), x.numel(), out.data_ptr(),
+                 workspace.data_ptr(), workspace.numel() * workspace.element_size())
     _check("rdx_reduce_ws", st)
     return out
 
@@ -248,8 +255,7 @@ def rdx_bank_probe(pattern: int, iters: int = 256, device=None, stream=None) -> 
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     cycles = torch.zeros(1, dtype=torch.int64, device=device)
     sink = torch.zeros(32, dtype=torch.int32, device=device)
-    with torch.cuda.device(device):
-        st = lib.rdx_bank_probe(pattern, iters, cycles.data_ptr(), sink.data_ptr(), _stream_handle(stream, device))
+    st = _launch(lib.rdx_bank_probe, device, stream, pattern, iters, cycles.data_ptr(), sink.data_ptr())
     _check("rdx_bank_probe", st)
     return cycles.item() / (iters * lib.rdx_bank_probe_loads_per_iter())
 
@@ -267,9 +273,7 @@ def rdx_ladder_partials_f32(version: int, x: torch.Tensor, out: torch.Tensor | N
     if nb < 0:
         raise ValueError(f"rdx_ladder_partials_f32: bad version {version}")
     out = _output(out, x, torch.float32, (nb,))
-    with torch.cuda.device(x.device):
-        st = lib.rdx_ladder_partials_f32(version, x.data_ptr(), x.numel(), out.data_ptr(),
-                                         _stream_handle(stream, x.device))
+    st = _launch(lib.rdx_ladder_partials_f32, x.device, stream, version, x.data_ptr(), x.numel(), out.data_ptr())
     _check("rdx_ladder_partials_f32", st)
     return out
 

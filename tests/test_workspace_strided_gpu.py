@@ -158,3 +158,32 @@ def test_row_offsets_past_2_to_the_32():
     assert abs(got[0] - cols) <= 1e-6 * cols and abs(got[1] + 0.25 * cols) <= 1e-6 * 0.25 * cols
     del x
     torch.cuda.empty_cache()
+
+
+def test_row_sums_replay_in_a_cuda_graph():
+    # the row kernels other than the split path use no workspace, so a capture
+    # on the current (capturing) stream with no stream argument replays them
+    shapes = [(50_000, 3), (20_000, 12), (20_000, 256), (3000, 2000), (3000, 16384)]
+    xs = [torch.empty(shape, device=DEV) for shape in shapes]
+    outs = [torch.empty(shape[0], device=DEV) for shape in shapes]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for x, o in zip(xs, outs):
+            abi.rdx_rowsum_f32(x.normal_(), out=o)  # warm-up
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for x, o in zip(xs, outs):
+            abi.rdx_rowsum_f32(x, out=o)
+    for seed in (21, 22):
+        hosts = []
+        for k, x in enumerate(xs):
+            host = inputs.uniform_f32(x.numel(), seed + k, lo=-1.0, hi=1.0).reshape(x.shape)
+            x.copy_(torch.from_numpy(host))
+            hosts.append(host)
+        g.replay()
+        torch.cuda.synchronize()
+        for host, o in zip(hosts, outs):
+            tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+            assert np.all(np.abs(o.cpu().numpy().astype(np.float64) - oracle.rowsum_f32(host)) <= tol)

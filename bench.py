@@ -433,6 +433,15 @@ def measure_extras(g: Gb300, per_config, iters):
     rows_out = torch.empty(4, dtype=torch.float32, device=g.dev)
     ms = g.time_launch(lambda: abi.rdx_rowsum_f32(xs, out=rows_out, stream=s), iters)
     extras["rowsum_4x67108864_split"] = figures(ms, 1 << 30)
+    # the maximum (the page's atomic_max rule) on the int32 1 GiB array and
+    # the fp32 64 MiB array: the same tiled kernel with a max fold
+    key3 = g.key(inputs.CFG3_SUM_I32)
+    for name, key, fn, dt in (("c3_max_i32", key3, abi.rdx_max_i32, torch.int32),
+                              ("c2_max_f32", key2, abi.rdx_max_f32, torch.float32)):
+        xk = g.dev_arrays[key]
+        om = torch.empty((), dtype=dt, device=g.dev)
+        ms = g.time_launch(lambda: fn(xk, out=om, stream=s), iters)
+        extras[name] = figures(ms, xk.numel() * xk.element_size())
     # narrow rows through shared memory: the same 1 GiB viewed as 3 and 12
     # columns (algorithmic bytes: 4 per element read and 4 per row written)
     flat = g.dev_arrays[g.key(inputs.CFG4_ROWSUM_WIDE)].view(-1)

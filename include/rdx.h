@@ -38,8 +38,9 @@
  * Float sums accumulate in float32 along a fixed tree (per-thread vector
  * folds, a warp shuffle tree, a cross-warp stage, and a fixed-order pass over
  * the block partials).  The order depends only on the input's length and its
- * 16-byte alignment (row sums: a row's address and length), never on timing
- * or on the GPU, so a repeated call gives the same bits.  Measured against
+ * 16-byte alignment (row sums: the matrix's shape and the alignment of its
+ * address), never on timing or on the GPU, so a repeated call gives the same
+ * bits.  Measured against
  * the exact sum, the error stays within 1e-6 * sum|x_i| for float32 input and
  * 4e-6 * sum|x_i| for bfloat16 input (sum of squares: the same factors times
  * sum x_i^2).  Inf and NaN propagate as in an IEEE sum.

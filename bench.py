@@ -456,13 +456,20 @@ def measure_extras(g: Gb300, per_config, iters):
 
 
 def measure_ladder(g: Gb300, iters):
-    """The page's five block reductions on the config-2 float32 array."""
+    """The page's five block reductions on the config-2 float32 array: the
+    partials alone (the page's kernel), and the whole sum with the device
+    finish in the same launch (comparable with c2_sum_f32)."""
     x2 = g.dev_arrays[g.key(inputs.CFG2_SUM_F32)]
+    nbytes = x2.numel() * 4
+    total = g.torch.empty((), dtype=g.torch.float32, device=g.dev)
     ladder = {}
     for v in range(1, 6):
         part = g.torch.empty(g.abi.rdx_ladder_num_partials(v, x2.numel()), dtype=g.torch.float32, device=g.dev)
         ms = g.time_launch(lambda: g.abi.rdx_ladder_partials_f32(v, x2, out=part, stream=g.stream), iters)
-        ladder[f"v{v}"] = {"us": round(ms * 1e3, 2), "GB/s": round(x2.numel() * 4 / (ms * 1e-3) / 1e9, 1)}
+        ms_sum = g.time_launch(lambda: g.abi.rdx_ladder_sum_f32(v, x2, out=total, partials=part, stream=g.stream),
+                               iters)
+        ladder[f"v{v}"] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                           "sum_us": round(ms_sum * 1e3, 2), "sum_GB/s": round(nbytes / (ms_sum * 1e-3) / 1e9, 1)}
     return ladder
 
 

@@ -227,6 +227,26 @@ rdx_status rdx_ladder_partials_f32(int version, const float* x, int64_t n, float
 int64_t rdx_ladder_num_partials(int version, int64_t n);
 
 /*
+ * rdx_ladder_sum_f32: *out = the sum of the partials of the page's block
+ * reduction `version`, finished on the device.  On the page (demo 3) the
+ * host adds the per-block partials after the kernel; here the same kernel
+ * also writes them to `partials` (bit for bit those of
+ * rdx_ladder_partials_f32) and then, in the same launch, the block that
+ * arrives last at the library's completion counter adds all of them in a
+ * fixed order into *out (the finish of rdx_sum_f32).  Each version thus
+ * becomes a complete sum that can be timed against rdx_sum_f32.
+ *   partials  rdx_ladder_num_partials(version, n) float32 values (scratch
+ *             the caller owns; holds the partials afterwards)
+ *   out       one float32; n == 0 writes 0.0f
+ * Uses the (device, stream) workspace's completion counter (allocated on the
+ * stream's first call, as for rdx_sum_f32).  Errors: as
+ * rdx_ladder_partials_f32, plus NULL, misaligned or overlapping `out`, and
+ * RDX_ERR_ALLOC if the workspace cannot be allocated.
+ */
+rdx_status rdx_ladder_sum_f32(int version, const float* x, int64_t n, float* partials, float* out,
+                              cudaStream_t stream);
+
+/*
  * rdx_sum_f32_noalloc: *out = sum_{i<n} x[i], like rdx_sum_f32, but the call
  * allocates no device memory.  (The paper, the pages this library follows,
  * has no counterpart: this entry point exists for callers of this library,

@@ -75,6 +75,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
+        lib.rdx_ladder_sum_f32.argtypes, lib.rdx_ladder_sum_f32.restype = [i32, vp, i64, vp, vp, vp], i32
         lib.rdx_status_string.argtypes, lib.rdx_status_string.restype = [i32], ctypes.c_char_p
         lib.rdx_last_cuda_error.argtypes, lib.rdx_last_cuda_error.restype = [], ctypes.c_char_p
         lib.rdx_shutdown.argtypes, lib.rdx_shutdown.restype = [], None
@@ -286,6 +287,24 @@ def rdx_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None, stream
     fn = lib.rdx_sum_f32_noalloc
     fn.argtypes, fn.restype = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int
     return _scalar("rdx_sum_f32_noalloc", x, (torch.float32,), torch.float32, out, stream)
+
+
+def rdx_ladder_sum_f32(version: int, x: torch.Tensor, out: torch.Tensor | None = None,
+                       partials: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the sum of a float32 tensor by the page's block
+    reduction ``version`` (1..5), its per-block partials (left in
+    ``partials``) added on the device in the same launch."""
+    lib = load()
+    x = _input(x, (torch.float32,), "rdx_ladder_sum_f32")
+    nb = lib.rdx_ladder_num_partials(version, x.numel())
+    if nb < 0:
+        raise ValueError(f"rdx_ladder_sum_f32: bad version {version}")
+    partials = _output(partials, x, torch.float32, (nb,))
+    out = _output(out, x, torch.float32, ())
+    st = _launch(lib.rdx_ladder_sum_f32, x.device, stream, version, x.data_ptr(), x.numel(), partials.data_ptr(),
+                 out.data_ptr())
+    _check("rdx_ladder_sum_f32", st)
+    return out
 
 
 def rdx_shutdown() -> None:

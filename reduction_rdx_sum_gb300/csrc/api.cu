@@ -259,7 +259,34 @@ rdx_status rdx_ladder_partials_f32(int version, const float* x, int64_t n, float
     const DeviceCaps* dev = nullptr;
     const rdx_status st = current_device(&dev);
     if (st != RDX_OK) return st;
-    const cudaError_t e = rdx::ladder_launch(version, x, n, partials, blocks, stream);
+    const cudaError_t e = rdx::ladder_launch(version, x, n, partials, blocks, nullptr, nullptr, stream);
+    if (e != cudaSuccess) return fail_cuda("ladder kernel launch", e);
+    return RDX_OK;
+}
+
+rdx_status rdx_ladder_sum_f32(int version, const float* x, int64_t n, float* partials, float* out,
+                              cudaStream_t stream) {
+    t_last_error.clear();
+    const int64_t blocks = rdx_ladder_num_partials(version, n);
+    if (blocks < 0) return RDX_ERR_INVALID_ARG;
+    if (blocks > 0x7fffffff) return RDX_ERR_INVALID_ARG;
+    if (out == nullptr || (n > 0 && (x == nullptr || partials == nullptr))) return RDX_ERR_INVALID_ARG;
+    if (!is_aligned(x, 4) || !is_aligned(partials, 4) || !is_aligned(out, 4)) return RDX_ERR_INVALID_ARG;
+    const size_t xb = size_t(n) * 4, pb = size_t(blocks) * 4;
+    if (overlaps(x, xb, partials, pb) || overlaps(x, xb, out, 4) || overlaps(partials, pb, out, 4))
+        return RDX_ERR_INVALID_ARG;
+
+    const DeviceCaps* dev = nullptr;
+    rdx_status st = current_device(&dev);
+    if (st != RDX_OK) return st;
+    if (blocks == 0) {
+        const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), stream);
+        return e == cudaSuccess ? RDX_OK : fail_cuda("cudaMemsetAsync of the result", e);
+    }
+    void* ws = nullptr;  // its first completion counter (stream order keeps users apart)
+    if ((st = stream_workspace(*dev, stream, &ws)) != RDX_OK) return st;
+    const cudaError_t e =
+        rdx::ladder_launch(version, x, n, partials, blocks, static_cast<unsigned*>(ws), out, stream);
     if (e != cudaSuccess) return fail_cuda("ladder kernel launch", e);
     return RDX_OK;
 }

@@ -264,6 +264,18 @@ __device__ __forceinline__ MaxAccI shfl_down(MaxAccI v, int off) {
     return MaxAccI(__shfl_down_sync(kFullMask, v.v, off));
 }
 
+// Completion counter of the last-block-done finish: acquire-release at GPU
+// scope, so the partial this thread stored before is visible to the block
+// that draws the last ticket, and that block sees every other block's partial.
+__device__ __forceinline__ unsigned take_ticket(unsigned* counter) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(counter), "r"(1u)
+                 : "memory");
+    return old;
+}
+
 // Loads of values other blocks wrote in this kernel: through L2 (ld.global.cg),
 // never a stale L1 line.
 __device__ __forceinline__ float load_cg(const float* p) { return __ldcg(p); }

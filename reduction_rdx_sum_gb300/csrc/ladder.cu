@@ -19,6 +19,10 @@
 // They are kept as the comparison ladder for the fast kernel in reduce.cu.
 // The page launches n / (B * per_thread) blocks and reads no index past the
 // end; here the last block may be partial and inputs past n count as 0.
+// The page adds the per-block partials on the host.  With kFinish the kernel
+// also finishes on the device, as the fast kernel does: every block stores
+// its partial and draws a ticket, and the block that draws the last one adds
+// all partials in a fixed order and writes the total.
 #include "device.cuh"
 #include "launch.h"
 
@@ -27,9 +31,12 @@ namespace {
 
 constexpr int B = kLadderBlock;
 
-template <int V>
+constexpr int kFinishChains = 8;  // partials in flight per thread in the finish
+
+template <int V, bool kFinish>
 __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in, int64_t n,
-                                                   float* __restrict__ out) {
+                                                   float* __restrict__ out, unsigned* __restrict__ counter,
+                                                   float* __restrict__ total) {
     __shared__ float sdata[B];
     const int tid = threadIdx.x;
     const int64_t bx = blockIdx.x;
@@ -71,11 +78,45 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
         if (tid < kWarpSize) {
             float val = sdata[tid] + sdata[tid + 32];
             for (int off = 16; off > 0; off >>= 1) val += __shfl_down_sync(kFullMask, val, off);
-            if (tid == 0 && guard(out + bx, 4, out, out_span)) out[bx] = val;
+            if (tid == 0) sdata[0] = val;  // thread 0 stores the partial below, as in versions 1-4
         }
-        return;
     }
+    // thread 0 holds the block's partial in sdata[0] (its own write, or one
+    // it saw before the last barrier)
     if (tid == 0 && guard(out + bx, 4, out, out_span)) out[bx] = sdata[0];
+    if (!kFinish) return;
+
+    // The device finish: thread 0 stored this block's partial and now draws
+    // a ticket (acquire-release), so the block with the last ticket sees
+    // every partial.  It adds them in a fixed order: thread t takes partials
+    // t, t + B, ... in kFinishChains independent chains, then a block tree.
+    __shared__ unsigned last_block;
+    __shared__ float warp_sums[B / kWarpSize];
+    if (tid == 0)
+        last_block = guard(counter, 4, counter, 4) ? take_ticket(counter) == gridDim.x - 1 : 0u;
+    __syncthreads();
+    if (!last_block) return;
+    const int64_t g = gridDim.x;
+    float acc[kFinishChains];
+#pragma unroll
+    for (int u = 0; u < kFinishChains; ++u) acc[u] = 0.f;
+    int64_t j = tid;
+    for (; j + (kFinishChains - 1) * B < g; j += kFinishChains * B) {
+        float p[kFinishChains];
+#pragma unroll
+        for (int u = 0; u < kFinishChains; ++u)
+            p[u] = guard(out + j + u * B, 4, out, out_span) ? load_cg(out + j + u * B) : 0.f;
+#pragma unroll
+        for (int u = 0; u < kFinishChains; ++u) acc[u] += p[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kFinishChains; ++u)
+        if (j + u * B < g && guard(out + j + u * B, 4, out, out_span)) acc[u] += load_cg(out + j + u * B);
+    const float sum = block_sum<B>(fold_array(acc), warp_sums, 0.f);
+    if (tid == 0) {
+        if (guard(total, 4, total, 4)) *total = sum;
+        if (guard(counter, 4, counter, 4)) *counter = 0u;  // ready for the next call on this stream
+    }
 }
 
 }  // namespace
@@ -83,18 +124,22 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
 RDX_DEFINE_VIOLATION_COUNTER(ladder_out_of_range)
 
 cudaError_t ladder_launch(int version, const float* x, int64_t n, float* partials, int64_t blocks,
-                          cudaStream_t stream) {
+                          unsigned* counter, float* total, cudaStream_t stream) {
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     const unsigned g = unsigned(blocks);
+#define RDX_LADDER(V)                                                                   \
+    (total ? ladder_kernel<V, true><<<g, B, 0, stream>>>(x, n, partials, counter, total) \
+           : ladder_kernel<V, false><<<g, B, 0, stream>>>(x, n, partials, counter, total))
     switch (version) {
-        case 1: ladder_kernel<1><<<g, B, 0, stream>>>(x, n, partials); break;
-        case 2: ladder_kernel<2><<<g, B, 0, stream>>>(x, n, partials); break;
-        case 3: ladder_kernel<3><<<g, B, 0, stream>>>(x, n, partials); break;
-        case 4: ladder_kernel<4><<<g, B, 0, stream>>>(x, n, partials); break;
-        case 5: ladder_kernel<5><<<g, B, 0, stream>>>(x, n, partials); break;
+        case 1: RDX_LADDER(1); break;
+        case 2: RDX_LADDER(2); break;
+        case 3: RDX_LADDER(3); break;
+        case 4: RDX_LADDER(4); break;
+        case 5: RDX_LADDER(5); break;
         default: return cudaErrorInvalidValue;
     }
+#undef RDX_LADDER
     return cudaGetLastError();
 }
 

@@ -81,7 +81,10 @@ void set_last_error(const char* text);
 
 // ---- the page's five block reductions (ladder.cu) --------------------------
 constexpr int kLadderBlock = 256;
+// partials: `blocks` floats.  With total != NULL the kernel also adds the
+// partials on the device into *total, using *counter (zero before the launch,
+// left zero after) as the completion counter.
 cudaError_t ladder_launch(int version, const float* x, int64_t n, float* partials, int64_t blocks,
-                          cudaStream_t stream);
+                          unsigned* counter, float* total, cudaStream_t stream);
 
 }  // namespace rdx

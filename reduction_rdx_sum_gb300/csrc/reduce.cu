@@ -65,18 +65,6 @@ static_assert((kUnroll & (kUnroll - 1)) == 0 && (kUnrollLarge & (kUnrollLarge - 
               "load batches are powers of two");
 static_assert(kMinTile % kBlock == 0, "tiles are whole multiples of the block");
 
-// Completion counter: acquire-release at GPU scope, so the partial this
-// thread stored before is visible to the block that draws the last ticket,
-// and that block sees every other block's partial.
-__device__ __forceinline__ unsigned take_ticket(unsigned* counter) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(counter), "r"(1u)
-                 : "memory");
-    return old;
-}
-
 template <class P, int U, int kMinBlocks>
 __global__ void __launch_bounds__(kBlock, kMinBlocks)
 reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, int64_t tile,

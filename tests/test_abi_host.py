@@ -88,6 +88,21 @@ def test_ladder_argument_validation(lib):
     assert n(0, 5) == -1 and n(1, -1) == -1
 
 
+def test_ladder_sum_argument_validation(lib):
+    f = lib.rdx_ladder_sum_f32
+    part, out = FAKE + 8192, FAKE + 16384
+    assert f(0, FAKE, 10, part, out, None) == INVALID                  # bad version
+    assert f(6, FAKE, 10, part, out, None) == INVALID
+    assert f(3, FAKE, -5, part, out, None) == INVALID                  # negative n
+    assert f(3, FAKE, 10, part, None, None) == INVALID                 # no output
+    assert f(3, None, 10, part, out, None) == INVALID                  # no input
+    assert f(3, FAKE, 10, None, out, None) == INVALID                  # no partials
+    assert f(3, FAKE, 10, part, out + 2, None) == INVALID              # output misaligned
+    assert f(3, FAKE, 1000, FAKE + 512, out, None) == INVALID          # partials inside x
+    assert f(3, FAKE, 1000, part, FAKE + 400, None) == INVALID         # output inside x
+    assert f(3, FAKE, 1000, part, part + 4, None) == INVALID           # output inside the partials
+
+
 def test_python_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(abi, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):

@@ -33,6 +33,7 @@ def lib():
     lib.rdx_rowsum_strided_f32.argtypes = [vp, i64, i64, i64, vp, vp]
     lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
     lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
+    lib.rdx_ladder_sum_f32.argtypes = [i32, vp, i64, vp, vp, vp]
     lib.rdx_debug_violations.argtypes = [vp, i32]
     lib.rdx_workspace_bytes.restype = ctypes.c_size_t
     for name in ("rdx_sum_f32", "rdx_sum_i32_i64", "rdx_max_f32"):
@@ -139,4 +140,19 @@ def test_ladder_stays_in_bounds(lib):
             assert lib.rdx_ladder_partials_f32(v, x.data_ptr(), n, out.data_ptr(), stream()) == 0
             torch.cuda.synchronize()
             assert np.array_equal(out.cpu().numpy(), oracle.ladder_partials(v, host))
+    assert violations(lib) == 0
+
+
+def test_ladder_sum_stays_in_bounds(lib):
+    for v in range(1, 6):
+        for n in (1, 257, 513, (1 << 16) + 77, (1 << 20) + 3):
+            host = inputs.normal_f32(n, seed=v + 9)
+            x = torch.from_numpy(host).to(DEV)
+            nb = lib.rdx_ladder_num_partials(v, n)
+            parts = torch.empty(nb, device=DEV)
+            out = torch.empty((), device=DEV)
+            assert lib.rdx_ladder_sum_f32(v, x.data_ptr(), n, parts.data_ptr(), out.data_ptr(), stream()) == 0
+            torch.cuda.synchronize()
+            assert np.array_equal(parts.cpu().numpy(), oracle.ladder_partials(v, host))
+            check("sum_f32", host, out.item())
     assert violations(lib) == 0

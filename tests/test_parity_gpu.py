@@ -338,6 +338,43 @@ def test_ladder_page_worked_example(version):
         assert float(got.astype(np.float64).sum()) == {1 << 14: 49146, 1 << 18: 786429}[n]
 
 
+@pytest.mark.parametrize("version", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("n", [0, 1, 255, 256, 257, 511, 513, 65537, (1 << 20) + 3, (1 << 24) + 13])
+def test_ladder_sum_with_device_finish(version, n):
+    # the partials are still the page's, bit for bit; their device-side sum
+    # is within the float tolerance of the oracle and repeats bit for bit
+    host = inputs.normal_f32(n, seed=version + 50)
+    x = torch.from_numpy(host).to(DEV)
+    parts = torch.full((max(1, abi.rdx_ladder_num_partials(version, n)),), float("nan"), device=DEV)
+    parts = parts[: abi.rdx_ladder_num_partials(version, n)]
+    out = abi.rdx_ladder_sum_f32(version, x, partials=parts)
+    assert np.array_equal(parts.cpu().numpy().view(np.uint32), oracle.ladder_partials(version, host).view(np.uint32))
+    check("sum_f32", host, out.item())
+    assert abi.rdx_ladder_sum_f32(version, x).view(torch.int32).item() == out.view(torch.int32).item()
+
+
+@pytest.mark.parametrize("version", [1, 2, 3, 4, 5])
+def test_ladder_sum_page_worked_example(version):
+    # in[i] = i mod 7: every partial and the total are exact integers
+    for n, total in ((1 << 14, 49146), (1 << 18, 786429)):
+        x = torch.from_numpy((np.arange(n) % 7).astype(np.float32)).to(DEV)
+        assert abi.rdx_ladder_sum_f32(version, x).item() == total
+
+
+def test_ladder_sum_interleaves_with_the_scalar_sums():
+    # the ladder's finish and the scalar sums share the stream's completion
+    # counter; each launch must leave it ready for the next
+    host = inputs.normal_f32((1 << 22) + 5, seed=77)
+    x = torch.from_numpy(host).to(DEV)
+    outs = []
+    for v in (1, 5, 3):
+        outs.append(abi.rdx_sum_f32(x))
+        outs.append(abi.rdx_ladder_sum_f32(v, x))
+    torch.cuda.synchronize()
+    for o in outs:
+        check("sum_f32", host, o.item())
+
+
 # ---------------------------------------------------------------------------
 # determinism, concurrency, limits, errors
 # ---------------------------------------------------------------------------

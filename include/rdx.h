@@ -233,7 +233,8 @@ int64_t rdx_ladder_num_partials(int version, int64_t n);
  * also writes them to `partials` (bit for bit those of
  * rdx_ladder_partials_f32) and then, in the same launch, the block that
  * arrives last at the library's completion counter adds all of them in a
- * fixed order into *out (the finish of rdx_sum_f32).  Each version thus
+ * fixed order into *out (the finish of rdx_sum_f32; the order depends on n,
+ * the version and the 16-byte alignment of `partials`).  Each version thus
  * becomes a complete sum that can be timed against rdx_sum_f32.
  *   partials  rdx_ladder_num_partials(version, n) float32 values (scratch
  *             the caller owns; holds the partials afterwards)

@@ -31,7 +31,7 @@ namespace {
 
 constexpr int B = kLadderBlock;
 
-constexpr int kFinishChains = 8;  // partials in flight per thread in the finish
+constexpr int kFinishLoads = 4;  // 16-byte loads of partials in flight per thread in the finish
 
 template <int V, bool kFinish>
 __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in, int64_t n,
@@ -86,10 +86,15 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
     if (tid == 0 && guard(out + bx, 4, out, out_span)) out[bx] = sdata[0];
     if (!kFinish) return;
 
-    // The device finish: thread 0 stored this block's partial and now draws
-    // a ticket (acquire-release), so the block with the last ticket sees
-    // every partial.  It adds them in a fixed order: thread t takes partials
-    // t, t + B, ... in kFinishChains independent chains, then a block tree.
+    // The device finish (last block done): thread 0 stored this block's
+    // partial and now draws a ticket (acquire-release), so the block with
+    // the last ticket sees every partial.  It adds them in a fixed order: the
+    // few before the first 16-byte boundary and after the last whole 16-byte
+    // vector one per thread; the vectors v = t, t + B, ... by thread t,
+    // kFinishLoads loads in flight, into one float4 of four chains; then a
+    // block tree.  Every block waits for its ticket before it exits: with
+    // blocks this short (one or two inputs per thread), that round trip is a
+    // large part of each block's life.
     __shared__ unsigned last_block;
     __shared__ float warp_sums[B / kWarpSize];
     if (tid == 0)
@@ -97,22 +102,26 @@ __global__ void __launch_bounds__(B) ladder_kernel(const float* __restrict__ in,
     __syncthreads();
     if (!last_block) return;
     const int64_t g = gridDim.x;
-    float acc[kFinishChains];
+    int64_t head = int64_t(((16u - (unsigned(reinterpret_cast<uintptr_t>(out)) & 15u)) & 15u) >> 2);
+    if (head > g) head = g;
+    const int64_t m = (g - head) >> 2;  // whole float4 vectors
+    const int64_t tail0 = head + 4 * m;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < head && guard(out + tid, 4, out, out_span)) acc.x += load_cg(out + tid);
+    if (tid < g - tail0 && guard(out + tail0 + tid, 4, out, out_span)) acc.y += load_cg(out + tail0 + tid);
+    const float4* __restrict__ ov = reinterpret_cast<const float4*>(out + head);
+    for (int64_t j = tid; j < m; j += kFinishLoads * B) {
+        float4 p[kFinishLoads];
 #pragma unroll
-    for (int u = 0; u < kFinishChains; ++u) acc[u] = 0.f;
-    int64_t j = tid;
-    for (; j + (kFinishChains - 1) * B < g; j += kFinishChains * B) {
-        float p[kFinishChains];
+        for (int u = 0; u < kFinishLoads; ++u)
+            p[u] = j + u * B < m && guard(ov + j + u * B, 16, out, out_span) ? __ldcg(ov + j + u * B)
+                                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < kFinishChains; ++u)
-            p[u] = guard(out + j + u * B, 4, out, out_span) ? load_cg(out + j + u * B) : 0.f;
-#pragma unroll
-        for (int u = 0; u < kFinishChains; ++u) acc[u] += p[u];
+        for (int u = 0; u < kFinishLoads; ++u) {
+            acc.x += p[u].x; acc.y += p[u].y; acc.z += p[u].z; acc.w += p[u].w;
+        }
     }
-#pragma unroll
-    for (int u = 0; u < kFinishChains; ++u)
-        if (j + u * B < g && guard(out + j + u * B, 4, out, out_span)) acc[u] += load_cg(out + j + u * B);
-    const float sum = block_sum<B>(fold_array(acc), warp_sums, 0.f);
+    const float sum = block_sum<B>((acc.x + acc.y) + (acc.z + acc.w), warp_sums, 0.f);
     if (tid == 0) {
         if (guard(total, 4, total, 4)) *total = sum;
         if (guard(counter, 4, counter, 4)) *counter = 0u;  // ready for the next call on this stream

@@ -345,12 +345,13 @@ def test_ladder_sum_with_device_finish(version, n):
     # is within the float tolerance of the oracle and repeats bit for bit
     host = inputs.normal_f32(n, seed=version + 50)
     x = torch.from_numpy(host).to(DEV)
-    parts = torch.full((max(1, abi.rdx_ladder_num_partials(version, n)),), float("nan"), device=DEV)
-    parts = parts[: abi.rdx_ladder_num_partials(version, n)]
+    nb, off = abi.rdx_ladder_num_partials(version, n), version % 2  # odd versions: partials 4 bytes off 16
+    parts = torch.full((nb + off,), float("nan"), device=DEV)[off:]
     out = abi.rdx_ladder_sum_f32(version, x, partials=parts)
     assert np.array_equal(parts.cpu().numpy().view(np.uint32), oracle.ladder_partials(version, host).view(np.uint32))
     check("sum_f32", host, out.item())
-    assert abi.rdx_ladder_sum_f32(version, x).view(torch.int32).item() == out.view(torch.int32).item()
+    again = abi.rdx_ladder_sum_f32(version, x, partials=parts)  # same buffers, same bits
+    assert again.view(torch.int32).item() == out.view(torch.int32).item()
 
 
 @pytest.mark.parametrize("version", [1, 2, 3, 4, 5])

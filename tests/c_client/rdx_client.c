@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <cuda_runtime_api.h>
 
@@ -44,9 +45,21 @@ int main(void) {
     int64_t sum_i = 0;
     for (int64_t i = (n / 2001) * 2001; i < n; ++i) sum_i += (i % 2001) - 1000; /* whole periods sum to 0 */
 
-    float *df, *dout, *drows, *dmax;
+    /* the same values as bfloat16 bit patterns (small integers: exact) */
+    rdx_bf16* hb = (rdx_bf16*)malloc((size_t)n * sizeof(rdx_bf16));
+    if (!hb) return 4;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        memcpy(&u, &hf[i], sizeof u);
+        hb[i] = (rdx_bf16)(u >> 16);
+    }
+    const int64_t rows3 = n / 3;                        /* narrow rows: 3 columns */
+    const int64_t nparts = rdx_ladder_num_partials(5, n);
+
+    float *df, *dout, *drows, *dmax, *drows3, *dparts, *dl5, *dbsum;
     int32_t *di, *dimax;
     int64_t* dsum_i;
+    rdx_bf16* db;
     void* ws;
     cudaStream_t s;
     CHECK_CUDA(cudaStreamCreate(&s));
@@ -57,6 +70,12 @@ int main(void) {
     CHECK_CUDA(cudaMalloc((void**)&dimax, sizeof(int32_t)));
     CHECK_CUDA(cudaMalloc((void**)&dsum_i, sizeof(int64_t)));
     CHECK_CUDA(cudaMalloc((void**)&drows, (size_t)rows * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&drows3, (size_t)rows3 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dparts, (size_t)nparts * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dl5, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dbsum, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&db, (size_t)n * sizeof(rdx_bf16)));
+    CHECK_CUDA(cudaMemcpy(db, hb, (size_t)n * sizeof(rdx_bf16), cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMalloc(&ws, rdx_workspace_bytes()));
     CHECK_CUDA(cudaMemset(ws, 0, rdx_workspace_bytes()));
     CHECK_CUDA(cudaMemcpy(df, hf, (size_t)n * sizeof(float), cudaMemcpyHostToDevice));
@@ -67,15 +86,24 @@ int main(void) {
     CHECK_RDX(rdx_max_f32(df, n, dmax, s));
     CHECK_RDX(rdx_max_i32(di, n, dimax, s));
     CHECK_RDX(rdx_rowsum_f32(df, rows, cols, drows, s));
+    CHECK_RDX(rdx_rowsum_f32(df, rows3, 3, drows3, s));
+    CHECK_RDX(rdx_ladder_sum_f32(5, df, n, dparts, dl5, s));
+    CHECK_RDX(rdx_sum_bf16_f32acc(db, n, dbsum, s));
     float got_f = 0.f, got_max = 0.f, pair[2] = {0.f, 0.f};
     int32_t got_imax = 0;
     int64_t got_i = 0;
+    float got_l5 = 0.f, got_b = 0.f;
     float* got_rows = (float*)malloc((size_t)rows * sizeof(float));
+    float* got_rows3 = (float*)malloc((size_t)rows3 * sizeof(float));
+    if (!got_rows || !got_rows3) return 4;
     CHECK_CUDA(cudaMemcpyAsync(&got_f, dout, sizeof(float), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaMemcpyAsync(&got_i, dsum_i, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaMemcpyAsync(&got_max, dmax, sizeof(float), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaMemcpyAsync(&got_imax, dimax, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaMemcpyAsync(got_rows, drows, (size_t)rows * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(got_rows3, drows3, (size_t)rows3 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_l5, dl5, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_b, dbsum, sizeof(float), cudaMemcpyDeviceToHost, s));
     CHECK_RDX(rdx_reduce_ws(RDX_OP_SUM_SUMSQ_F32, df, n, dout, ws, rdx_workspace_bytes(), s));
     CHECK_CUDA(cudaMemcpyAsync(pair, dout, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaStreamSynchronize(s));
@@ -85,6 +113,12 @@ int main(void) {
     if (got_i != sum_i) { fprintf(stderr, "sum_i32 %lld != %lld\n", (long long)got_i, (long long)sum_i); bad = 1; }
     if (got_max != 6.f || got_imax != 1000) { fprintf(stderr, "max %g %d\n", got_max, got_imax); bad = 1; }
     if ((double)pair[0] != sum_f) { fprintf(stderr, "ws pair sum %.1f\n", pair[0]); bad = 1; }
+    if ((double)got_l5 != sum_f) { fprintf(stderr, "ladder v5 sum %.1f != %.1f\n", got_l5, sum_f); bad = 1; }
+    if ((double)got_b != sum_f) { fprintf(stderr, "bf16 sum %.1f != %.1f\n", got_b, sum_f); bad = 1; }
+    for (int64_t row = 0; row < rows3 && !bad; ++row) {
+        const double e = (double)hf[3 * row] + (double)hf[3 * row + 1] + (double)hf[3 * row + 2];
+        if ((double)got_rows3[row] != e) { fprintf(stderr, "3-column row %lld\n", (long long)row); bad = 1; }
+    }
     for (int64_t row = 0; row < rows && !bad; ++row) {
         double e = 0.0;
         for (int64_t j = 0; j < cols; ++j) e += (double)hf[row * cols + j];

@@ -28,7 +28,11 @@
  *    reused after.  Make that first call outside any CUDA-graph capture, or
  *    pass a workspace of your own to rdx_reduce_ws.  Two host threads may
  *    call concurrently; calls on one stream are ordered by the stream.
- *    rdx_shutdown() frees the library's workspaces.
+ *    cudaStreamPerThread gets one workspace per host thread (it names a
+ *    different stream in each).  A workspace is found by the stream's handle:
+ *    synchronize a stream before destroying it, or a new stream that is
+ *    given the same handle could share the workspace with work still
+ *    pending.  rdx_shutdown() frees the library's workspaces.
  *  - Errors: no exception crosses this ABI.  Each call returns an rdx_status;
  *    argument errors are found before any CUDA call and nothing is enqueued.
  *    After RDX_ERR_CUDA, rdx_last_cuda_error() names the failing CUDA call.

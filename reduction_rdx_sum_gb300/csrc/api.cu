@@ -5,10 +5,12 @@
 
 #include <climits>
 #include <cstdlib>
+#include <functional>
 #include <map>
 #include <mutex>
 #include <string>
-#include <utility>
+#include <thread>
+#include <tuple>
 
 #include "device.cuh"  // RDX_DEBUG
 #include "launch.h"
@@ -27,7 +29,10 @@ rdx_status fail_cuda(const char* what, cudaError_t e) {
 
 std::mutex g_mu;
 std::map<int, DeviceCaps> g_caps;                          // by device ordinal
-std::map<std::pair<int, uintptr_t>, void*> g_workspaces;  // by (device, stream)
+// by (device, stream, host thread): cudaStreamPerThread names a different
+// stream in every host thread, so its workspaces are kept per thread (the
+// thread part of the key is 0 for every other stream)
+std::map<std::tuple<int, uintptr_t, size_t>, void*> g_workspaces;
 
 // Workspace layout: [completion counters: one per row, kMaxSplitRows of them]
 // [tile partials: reduce_max_partials() slots of 8 bytes].  The counters must
@@ -73,7 +78,9 @@ rdx_status current_device(const DeviceCaps** out) {
 // partial slots poisoned (in stream order) on first use.
 rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    const auto key = std::make_pair(dev.ordinal, reinterpret_cast<uintptr_t>(stream));
+    const size_t thread_key =
+        stream == cudaStreamPerThread ? std::hash<std::thread::id>{}(std::this_thread::get_id()) | 1u : 0u;
+    const auto key = std::make_tuple(dev.ordinal, reinterpret_cast<uintptr_t>(stream), thread_key);
     auto it = g_workspaces.find(key);
     if (it != g_workspaces.end()) {
         *out = it->second;

@@ -470,6 +470,41 @@ def test_overlap_and_bad_tensors_rejected():
     assert abi.rdx_sum_f32(x).item() == 1000.0
 
 
+def test_per_thread_default_stream_gets_a_workspace_per_thread():
+    # cudaStreamPerThread (handle 2) is a different stream in every host
+    # thread; calls from several threads at once must not share a workspace
+    import threading
+
+    lib = abi.load()
+    per_thread = 2
+    hosts = [inputs.normal_f32((1 << 22) + 31 * i, seed=60 + i) for i in range(4)]
+    devs = [torch.from_numpy(h).to(DEV) for h in hosts]
+    outs = [[torch.empty((), device=DEV) for _ in range(25)] for _ in hosts]
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(DEV)
+            for o in outs[i]:
+                st = lib.rdx_sum_f32(devs[i].data_ptr(), devs[i].numel(), o.data_ptr(), per_thread)
+                if st != 0:
+                    errors.append(st)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(hosts))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for h, row in zip(hosts, outs):
+        assert len({o.view(torch.int32).item() for o in row}) == 1  # every call the same bits
+        check("sum_f32", h, row[0].item())
+
+
 def test_host_threads_call_concurrently():
     # ctypes drops the GIL during a call: several host threads enqueue on
     # their own streams at once (per-stream workspaces, no shared state)

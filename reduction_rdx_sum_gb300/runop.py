@@ -4,6 +4,7 @@ For quick timings and for profilers (one kernel, a few launches, a chosen size):
 
     python -m reduction_rdx_sum_gb300.runop --op sum_bf16 --n 268435456 --iters 3
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 262144 --cols 256
+    python -m reduction_rdx_sum_gb300.runop --config c5_sum_bf16     # a workload of the suite
 
 Before each timed call the L2 is flushed (a write of 512 MiB, then a read of
 512 MiB so that no dirty line is left for the timed kernel to write back).
@@ -60,7 +61,9 @@ class L2Flush:
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
-    ap.add_argument("--op", choices=OPS, required=True)
+    ap.add_argument("--op", choices=OPS)
+    ap.add_argument("--config", choices=[w.name for w in inputs.ALL],
+                    help="run one workload of the five configurations (its op, shape and seeded input)")
     ap.add_argument("--n", type=int, default=1 << 28)
     ap.add_argument("--rows", type=int, default=8192)
     ap.add_argument("--cols", type=int, default=32768)
@@ -68,6 +71,8 @@ def main(argv=None) -> int:
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-flush", action="store_true")
     args = ap.parse_args(argv)
+    if (args.op is None) == (args.config is None):
+        ap.error("give exactly one of --op and --config")
 
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
@@ -77,7 +82,14 @@ def main(argv=None) -> int:
             c = abi.rdx_bank_probe(pattern, iters=max(1, args.iters), device=dev)
             print(json.dumps({"op": "bank_probe", "pattern": pattern, "cycles_per_load": round(c, 2)}), flush=True)
         return 0
-    x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
+    if args.config is not None:
+        w = {w.name: w for w in inputs.ALL}[args.config]
+        host = inputs.make(w)
+        host = host.view(np.int16) if host.dtype == np.uint16 else host
+        x = torch.from_numpy(host.reshape(w.shape)).to(dev)
+        args.op = w.op
+    else:
+        x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
     fn = entry(args.op)
     stream = torch.cuda.current_stream(dev)
     flush = None if args.no_flush else L2Flush(dev)

@@ -310,9 +310,14 @@ def test_rowsum_page_segments():
     n = 1 << 18
     x = (np.arange(n) % 7).astype(np.float32)
     period = {256: [762, 771, 766, 768, 770, 765, 774], 512: [1533, 1534, 1535, 1536, 1537, 1538, 1539]}
+    xt = torch.from_numpy(x).to(DEV)
     for seg, p in period.items():
-        got = abi.rdx_rowsum_f32(torch.from_numpy(x.reshape(-1, seg)).to(DEV)).cpu().tolist()
+        got = abi.rdx_rowsum_f32(xt.view(-1, seg)).cpu().tolist()
         assert got == [p[b % 7] for b in range(n // seg)]
+        # a row of B (2B) inputs is exactly the segment a block of versions
+        # 1-3 (4-5) reduces: the row sums equal those versions' partials
+        for v in ((1, 2, 3) if seg == 256 else (4, 5)):
+            assert abi.rdx_ladder_partials_f32(v, xt).cpu().tolist() == got
 
 
 # ---------------------------------------------------------------------------

@@ -22,8 +22,9 @@
  *  - Any element-aligned input pointer is accepted; 16-byte alignment is not
  *    required.  The output must not overlap the input.
  *  - Scratch: the scalar reductions (and the row sum of few, very long rows)
- *    keep one small workspace per (device, stream) pair (tile partials and
- *    completion counters, rdx_workspace_bytes() bytes), allocated by the
+ *    keep one small workspace per (device, stream) pair (tile partials,
+ *    completion counters and, for the exact integer reductions, one
+ *    accumulator word; rdx_workspace_bytes() bytes), allocated by the
  *    library with cudaMalloc on the first call on that pair that needs it and
  *    reused after.  Make that first call outside any CUDA-graph capture, or
  *    pass a workspace of your own to rdx_reduce_ws.  Two host threads may

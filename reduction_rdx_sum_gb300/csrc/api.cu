@@ -35,12 +35,30 @@ std::map<int, DeviceCaps> g_caps;                          // by device ordinal
 std::map<std::tuple<int, uintptr_t, size_t>, void*> g_workspaces;
 
 // Workspace layout: [completion counters: one per row, kMaxSplitRows of them]
-// [tile partials: reduce_max_partials() slots of 8 bytes].  The counters must
-// be zero before a launch; every launch leaves them zero.
+// [accumulator word of the exact integer reductions, padded to 256 bytes]
+// [tile partials: reduce_max_partials() slots of 8 bytes].  The counters and
+// the word must be zero before a launch; every launch leaves them zero.
 constexpr size_t kCounterBytes = size_t(rdx::kMaxSplitRows) * sizeof(unsigned);
-static_assert(kCounterBytes % 256 == 0, "partials start 256-byte aligned");
+constexpr size_t kWordBytes = 256;
+constexpr size_t kZeroBytes = kCounterBytes + kWordBytes;  // the part that starts zeroed
+static_assert(kCounterBytes % 256 == 0 && kZeroBytes % 256 == 0, "word and partials start 256-byte aligned");
 
-size_t workspace_bytes() { return kCounterBytes + size_t(rdx::reduce_max_partials()) * 8; }
+size_t workspace_bytes() { return kZeroBytes + size_t(rdx::reduce_max_partials()) * 8; }
+
+struct WorkspaceParts {
+    unsigned* counters = nullptr;
+    unsigned long long* words = nullptr;
+    void* partials = nullptr;
+};
+WorkspaceParts parts_of(void* ws) {
+    WorkspaceParts p;
+    if (ws != nullptr) {
+        p.counters = static_cast<unsigned*>(ws);
+        p.words = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + kCounterBytes);
+        p.partials = static_cast<char*>(ws) + kZeroBytes;
+    }
+    return p;
+}
 
 bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
@@ -98,11 +116,11 @@ rdx_status stream_workspace(const DeviceCaps& dev, cudaStream_t stream, void** o
         t_last_error = std::string("cudaMalloc of the workspace: ") + cudaGetErrorString(e);
         return RDX_ERR_ALLOC;
     }
-    e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
+    e = cudaMemsetAsync(p, 0, kZeroBytes, stream);
     // Poison the partial slots (all-ones bytes: a NaN for float slots): a
     // partial read before it was written would show up in the result.
-    if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<char*>(p) + kCounterBytes, 0xFF,
-                                              workspace_bytes() - kCounterBytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<char*>(p) + kZeroBytes, 0xFF,
+                                              workspace_bytes() - kZeroBytes, stream);
     if (e != cudaSuccess) {
         cudaFree(p);
         return fail_cuda("cudaMemsetAsync of the workspace", e);
@@ -127,9 +145,8 @@ rdx_status check_scalar(Op op, const void* x, int64_t n, const void* out) {
 // One row of n elements; ws is the workspace (NULL when the plan has one tile).
 rdx_status launch_scalar(Op op, const void* x, int64_t n, void* out, void* ws, cudaStream_t stream) {
     const rdx::ReducePlan plan = rdx::reduce_plan(op, 1, n);
-    unsigned* counters = static_cast<unsigned*>(ws);
-    void* partials = ws ? static_cast<char*>(ws) + kCounterBytes : nullptr;
-    const cudaError_t e = rdx::reduce_launch(op, x, 1, n, n, plan, partials, counters, out, stream);
+    const WorkspaceParts w = parts_of(ws);
+    const cudaError_t e = rdx::reduce_launch(op, x, 1, n, n, plan, w.partials, w.counters, w.words, out, stream);
     if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
     return RDX_OK;
 }
@@ -166,9 +183,9 @@ rdx_status rowsum_entry(const float* x, int64_t rows, int64_t cols, int64_t ld, 
         const rdx::ReducePlan plan = rdx::reduce_plan(Op::SumF32, rows, cols);
         void* ws = nullptr;
         if ((st = stream_workspace(*dev, stream, &ws)) != RDX_OK) return st;
+        const WorkspaceParts w = parts_of(ws);
         const cudaError_t e =
-            rdx::reduce_launch(Op::SumF32, x, rows, cols, ld, plan, static_cast<char*>(ws) + kCounterBytes,
-                               static_cast<unsigned*>(ws), out, stream);
+            rdx::reduce_launch(Op::SumF32, x, rows, cols, ld, plan, w.partials, w.counters, nullptr, out, stream);
         if (e != cudaSuccess) return fail_cuda("split-row kernel launch", e);
         return RDX_OK;
     }

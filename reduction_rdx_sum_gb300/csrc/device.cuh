@@ -87,6 +87,25 @@ struct is_exact<P, decltype(void(P::kExact))> {
     static constexpr bool value = P::kExact;
 };
 
+// Integer reductions whose result has the same bits in any order (int64
+// addition, which is addition modulo 2^64, and the maximum) may finish
+// through one 8-byte accumulator word per row instead of block partials:
+// every block folds its total in with a fire-and-forget atomic, and the
+// block that draws the last ticket takes the word (reading it and leaving it
+// zero).  Such a policy declares kWordFinish and provides
+//   fold_word(word, acc)  atomically fold a block total into the word;
+//   take_word(word)       atomically read the word, reset it to zero, and
+//                         return the result it holds (zero stands for the
+//                         policy's identity).
+template <class P, class = void>
+struct has_word_finish {
+    static constexpr bool value = false;
+};
+template <class P>
+struct has_word_finish<P, decltype(void(P::kWordFinish))> {
+    static constexpr bool value = P::kWordFinish;
+};
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -157,6 +176,12 @@ struct SumI32 {
     __device__ static Acc fold(uint4 v) {
         return (Acc(int32_t(v.x)) + Acc(int32_t(v.y))) + (Acc(int32_t(v.z)) + Acc(int32_t(v.w)));
     }
+    // the word holds the running int64 sum (its two's-complement bits)
+    static constexpr bool kWordFinish = true;
+    __device__ static void fold_word(unsigned long long* w, Acc a) {
+        atomicAdd(w, static_cast<unsigned long long>(a));  // result unused: a reduction (red), no round trip
+    }
+    __device__ static Acc take_word(unsigned long long* w) { return static_cast<Acc>(atomicExch(w, 0ull)); }
 };
 
 // Sum and sum of squares carried together (one pass over the input for both).
@@ -248,6 +273,16 @@ struct MaxI32 {
     __device__ static Acc fold(uint4 v) {
         return Acc(max(max(int(v.x), int(v.y)), max(int(v.z), int(v.w))));
     }
+    // The word holds the running maximum as an unsigned key: the value with
+    // its sign bit flipped, which orders as the signed value does and maps
+    // the identity -2^31 to zero.
+    static constexpr bool kWordFinish = true;
+    __device__ static void fold_word(unsigned long long* w, Acc a) {
+        atomicMax(w, static_cast<unsigned long long>(static_cast<unsigned>(a.v) ^ 0x80000000u));
+    }
+    __device__ static Acc take_word(unsigned long long* w) {
+        return Acc(static_cast<int>(static_cast<unsigned>(atomicExch(w, 0ull)) ^ 0x80000000u));
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -302,6 +337,27 @@ __device__ __forceinline__ T warp_sum(T v) {
     for (int off = kWarpSize / 2; off > 0; off >>= 1) v += shfl_down(v, off);
     return v;
 }
+
+// The exact integer trees run on the warp's 32-bit reduce unit (redux.sync,
+// one instruction per 32 lanes) instead of five shuffle steps; every lane
+// ends with the result.
+//
+// int64 sum: each lane's value, read as 64 unsigned bits, is cut into its
+// high word and two 16-bit low parts.  32 parts of 16 bits add up to less
+// than 2^21, so those two sums are exact; the high words' sum wraps modulo
+// 2^32, which loses nothing, because it is weighted by 2^32 and int64
+// (two's-complement) addition is itself addition modulo 2^64.
+__device__ __forceinline__ long long warp_sum(long long v) {
+    const unsigned long long u = static_cast<unsigned long long>(v);
+    const unsigned hi = __reduce_add_sync(kFullMask, unsigned(u >> 32));
+    const unsigned mid = __reduce_add_sync(kFullMask, unsigned(u >> 16) & 0xffffu);
+    const unsigned lo = __reduce_add_sync(kFullMask, unsigned(u) & 0xffffu);
+    return static_cast<long long>((static_cast<unsigned long long>(hi) << 32) +
+                                  (static_cast<unsigned long long>(mid) << 16) + lo);
+}
+
+// int32 maximum: the reduce unit's signed maximum.
+__device__ __forceinline__ MaxAccI warp_sum(MaxAccI v) { return MaxAccI(__reduce_max_sync(kFullMask, v.v)); }
 
 // Every lane of each aligned group of `width` lanes ends with the group's sum.
 // In the xor butterfly both partners add the same two values, so all lanes of

@@ -47,11 +47,17 @@ int reduce_vec_elems(Op op);
 size_t reduce_elem_bytes(Op op);
 size_t reduce_acc_bytes(Op op);
 ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols);
-// partials: rows * plan.tiles slots (reduce_acc_bytes each); counters: rows
-// zeroed completion counters, left zeroed.  Neither is touched when
-// plan.tiles == 1.  out: rows results.
+// Whether `op` finishes through an accumulator word instead of partials (the
+// exact integer reductions; rows must then be 1).
+bool reduce_uses_words(Op op);
+// partials: rows * plan.tiles slots (reduce_acc_bytes each; not touched by
+// the word-finishing ops); counters: rows zeroed completion counters, left
+// zeroed; words: one zeroed 8-byte accumulator word, left zeroed (only the
+// word-finishing ops touch it; it may be NULL for the others).  None of these
+// is touched when plan.tiles == 1.  out: rows results.
 cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
-                          void* partials, unsigned* counters, void* out, cudaStream_t stream);
+                          void* partials, unsigned* counters, unsigned long long* words, void* out,
+                          cudaStream_t stream);
 
 // ---- row-segmented sum (rowsum.cu) ----------------------------------------
 // Rows of `cols` elements starting every `ld` elements; no workspace.

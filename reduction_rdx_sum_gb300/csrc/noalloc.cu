@@ -120,7 +120,7 @@ extern "C" rdx_status rdx_sum_f32_noalloc(const float* x, int64_t n, float* out,
     cudaError_t e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
     if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync of the completion counter", e);
     e = rdx::reduce_launch(rdx::Op::SumF32, x, 1, n, n, plan, scratch + kCounterBytes,
-                           reinterpret_cast<unsigned*>(scratch), out, stream);
+                           reinterpret_cast<unsigned*>(scratch), nullptr, out, stream);
     if (e != cudaSuccess) return fail_cuda("reduce kernel launch", e);
     return RDX_OK;
 }

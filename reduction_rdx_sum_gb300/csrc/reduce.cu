@@ -21,7 +21,10 @@
 //   * the tile partials are finished on the device: the block that arrives
 //     last at a completion counter (acquire-release atomic) adds all partials
 //     in a fixed order and resets the counter.  Nothing waits on anything,
-//     and no float atomics are used.
+//     and no float atomics are used.  The exact integer reductions (int64
+//     sum, int32 maximum), whose result has the same bits in any order, fold
+//     each block total into one accumulator word with an integer atomic
+//     instead, and the last block only reads that word back.
 // The same kernel sums the rows of a matrix with few, long rows: gridDim.y
 // rows, each cut into tiles with its own completion counter and partials;
 // the scalar reductions are the one-row case.
@@ -69,7 +72,7 @@ template <class P, int U, int kMinBlocks>
 __global__ void __launch_bounds__(kBlock, kMinBlocks)
 reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, int64_t tile,
               typename P::Acc* __restrict__ partials, unsigned* __restrict__ counters,
-              typename P::Acc* __restrict__ out) {
+              unsigned long long* __restrict__ words, typename P::Acc* __restrict__ out) {
     using Acc = typename P::Acc;
     constexpr int V = P::kVec;
     __shared__ Acc smem[kBlock / kWarpSize];
@@ -129,8 +132,26 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
         if (threadIdx.x == 0 && guard(out + row, sizeof(Acc), out, out_span)) out[row] = a;
         return;
     }
-    Acc* __restrict__ rp = partials + row * int64_t(gridDim.x);
     unsigned* counter = counters + row;
+    if constexpr (has_word_finish<P>::value) {
+        // Exact integer reductions: the block total goes into the row's
+        // accumulator word (a fire-and-forget atomic, released by the ticket
+        // that follows it); the block with the last ticket takes the word.
+        // One thread does it all: no partial is stored or read again.
+        if (threadIdx.x == 0) {
+            unsigned long long* word = words + row;
+            const size_t word_span = size_t(gridDim.y) * sizeof(unsigned long long);
+            if (guard(word, sizeof *word, words, word_span)) P::fold_word(word, a);
+            if (guard(counter, sizeof(unsigned), counters, gridDim.y * sizeof(unsigned)) &&
+                take_ticket(counter) == gridDim.x - 1) {
+                const Acc total = guard(word, sizeof *word, words, word_span) ? P::take_word(word) : P::identity();
+                if (guard(out + row, sizeof(Acc), out, out_span)) out[row] = total;
+                *counter = 0u;  // ready for the next call on this stream (checked above)
+            }
+        }
+        return;
+    }
+    Acc* __restrict__ rp = partials + row * int64_t(gridDim.x);
     const size_t part_span = size_t(gridDim.x) * gridDim.y * sizeof(Acc);
     if (threadIdx.x == 0) {
         if (guard(rp + blockIdx.x, sizeof(Acc), partials, part_span)) rp[blockIdx.x] = a;
@@ -173,17 +194,18 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
 
 template <class P>
 cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
-                         void* partials, unsigned* counters, void* out, cudaStream_t stream) {
+                         void* partials, unsigned* counters, unsigned long long* words, void* out,
+                         cudaStream_t stream) {
     const dim3 grid(unsigned(plan.tiles), unsigned(rows));
     const auto* xt = static_cast<const typename P::In*>(x);
     auto* pt = static_cast<typename P::Acc*>(partials);
     auto* ot = static_cast<typename P::Acc*>(out);
     if (plan.large)
         reduce_kernel<P, kUnrollLarge, kMinBlocksLarge><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
-                                                                                     counters, ot);
+                                                                                     counters, words, ot);
     else
         reduce_kernel<P, kUnroll, kMinBlocksPerSm><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
-                                                                                counters, ot);
+                                                                                counters, words, ot);
     return cudaGetLastError();
 }
 
@@ -232,9 +254,14 @@ ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     return p;
 }
 
+bool reduce_uses_words(Op op) { return op == Op::SumI32 || op == Op::MaxI32; }
+
 cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
-                          void* partials, unsigned* counters, void* out, cudaStream_t stream) {
-#define RDX_LAUNCH(P) launch_typed<P>(x, rows, cols, ld, plan, partials, counters, out, stream)
+                          void* partials, unsigned* counters, unsigned long long* words, void* out,
+                          cudaStream_t stream) {
+    // the word finish serves one row (the scalar reductions)
+    if (reduce_uses_words(op) && plan.tiles > 1 && (rows != 1 || words == nullptr)) return cudaErrorInvalidValue;
+#define RDX_LAUNCH(P) launch_typed<P>(x, rows, cols, ld, plan, partials, counters, words, out, stream)
     switch (op) {
         case Op::SumF32: return RDX_LAUNCH(SumF32);
         case Op::SumSqF32: return RDX_LAUNCH(SumSqF32);

@@ -137,6 +137,26 @@ def test_integer_extremes_exact():
         assert abi.rdx_sum_i32_i64(x).item() == v * n
 
 
+def test_integer_accumulator_word_left_clear_between_ops():
+    # The int64 sum and the int32 maximum finish through one accumulator word
+    # of the stream's workspace; every call must leave it clear for the next,
+    # whichever op comes next.  All -2^31 is the maximum whose word key is 0.
+    hosts = [inputs.integers_i32((1 << 22) + k, seed=40 + k, lo=-(2 ** 31), hi=2 ** 31 - 1) for k in range(3)]
+    xs = [to_device(h, offset=k) for k, h in enumerate(hosts)]
+    low = torch.full(((1 << 20) + 3,), -(2 ** 31), dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream()
+    for rep in range(3):
+        for h, x in zip(hosts, xs):
+            assert abi.rdx_sum_i32_i64(x).item() == oracle.sum_i32(h)
+            assert abi.rdx_max_i32(x).item() == oracle.max_i32(h)
+        assert abi.rdx_max_i32(low).item() == -(2 ** 31)
+        assert abi.rdx_sum_i32_i64(low).item() == -(2 ** 31) * low.numel()
+        with torch.cuda.stream(side):
+            got = abi.rdx_max_i32(xs[rep], stream=side)
+        side.synchronize()
+        assert got.item() == oracle.max_i32(hosts[rep])
+
+
 def test_nonfinite_propagation():
     n = 100_003
     for pos in (0, 5, n // 2, n - 1):

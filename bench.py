@@ -54,21 +54,21 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "919007bc5a8c3321"
-_ROW_HASH = "e41c96e93516b497"
+_RED_HASH = "16eda084cc686085"
+_ROW_HASH = "14e4e89bb268c8e0"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2160294926, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2161143822, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2159250446, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2159154190, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1079549952, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1079365120, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67260416, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67246592, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079979520, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1080093184, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086093312, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1085933568, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

@@ -41,6 +41,10 @@ constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight
 constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
 constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
 constexpr int64_t kNarrowMaxCols = 64;   // narrow rows: fewer columns than this
+// Rotated reads (see rowsum_narrow_kernel) pay one shared load per VEC-float
+// group of a row; measured against the short-row kernel, they win up to 52
+// groups (1-float reads of 56 columns tie, of 60 columns lose).
+constexpr int kRotatedMaxGroups = 52;
 
 // Elements of a row before its first 16-byte boundary (rows of a matrix with
 // cols % 4 != 0 start at varying alignments).
@@ -218,11 +222,16 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 // so a row's sum is VEC chains of every VEC-th term, added at the end (two
 // chains of alternate terms for VEC = 1).  Rows start every cols words:
 // with VEC = 1 for odd cols, VEC = 2 for cols = 2 (mod 4) and VEC = 4 for
-// cols = 4 (mod 8), a warp's reads meet no bank conflict; the launcher
-// (rowsum_use_narrow) takes this kernel only where they share a bank at most
-// 2 ways (4 ways for 8 columns or fewer).  The order depends only on cols and
-// VEC.
-template <int VEC>
+// cols = 4 (mod 8), a warp's reads meet no bank conflict.  Where rows that
+// start cols words apart would share banks (cols with a large power of two,
+// read 1 or 2 floats at a time: rows that are not 16-byte aligned), ROT
+// rotates each lane's reads: lane l starts its row at VEC-float group
+// l mod (cols / VEC) and wraps around, so the 32 lanes of a step read
+// different columns.  The launcher (rowsum_narrow_read) takes this kernel
+// only where the reads share a bank at most 2 ways (4 ways for 8 columns or
+// fewer), and rotated reads only up to kRotatedMaxGroups loads per row.  The order depends only on cols, VEC, ROT and, with ROT, the row's
+// lane (its index modulo 32).
+template <int VEC, bool ROT>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
                      float* __restrict__ out) {
@@ -261,7 +270,32 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     for (int q = t; q < nr; q += kNarrowBlock) {
         const float* row = tile + s + q * ci;
         float sum;
-        if (VEC == 4) {
+        if (ROT) {
+            // VEC-float groups k0, k0 + 1, ..., wrapping at the row's end
+            constexpr int kLanes = kWarpSize;
+            const int w = ci / VEC;
+            int k = (t % kLanes) % w;
+            if (VEC == 2) {
+                float2 a = make_float2(0.f, 0.f);
+                for (int j = 0; j < w; ++j) {
+                    const float2 e = *reinterpret_cast<const float2*>(row + 2 * k);
+                    a.x += e.x; a.y += e.y;
+                    k = k + 1 == w ? 0 : k + 1;
+                }
+                sum = a.x + a.y;
+            } else {
+                float a0 = 0.f, a1 = 0.f;
+                int j = 0;
+                for (; j + 1 < w; j += 2) {
+                    a0 += row[k];
+                    k = k + 1 == w ? 0 : k + 1;
+                    a1 += row[k];
+                    k = k + 1 == w ? 0 : k + 1;
+                }
+                if (j < w) a0 += row[k];
+                sum = a0 + a1;
+            }
+        } else if (VEC == 4) {
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < ci; j += 4) {
                 const float4 e = *reinterpret_cast<const float4*>(row + j);
@@ -334,6 +368,38 @@ bool rowsum_use_split(int64_t rows, int64_t cols) {
     return rows <= kMaxSplitRows && cols >= 16384;
 }
 
+// Worst shared-memory bank sharing of the narrow kernel's row reads.  The 32
+// lanes of a warp sum rows that start cols words apart, VEC words at a time;
+// in step j lane l reads VEC-word group j of its row, or (rotated) group
+// (j + l) mod (cols / VEC).  The figure is the most words one bank serves in
+// any step, over VEC (a VEC-word read takes VEC banks per lane), rounded up.
+static int narrow_bank_ways(int cols, int vec, bool rotated) {
+    const int w = cols / vec;
+    int worst = 0;
+    for (int j = 0; j < w; ++j) {
+        int count[kWarpSize] = {};
+        for (int lane = 0; lane < kWarpSize; ++lane) {
+            const int k = rotated ? (j + lane) % w : j;
+            for (int e = 0; e < vec; ++e) ++count[(lane * cols + k * vec + e) % kWarpSize];
+        }
+        for (int b = 0; b < kWarpSize; ++b) worst = worst > (count[b] + vec - 1) / vec ? worst : (count[b] + vec - 1) / vec;
+    }
+    return worst;
+}
+
+// narrow_bank_ways for every narrow width and read width, worked out once.
+struct NarrowWays {
+    unsigned char ways[kNarrowMaxCols][3][2] = {};  // [cols][vec 1, 2, 4 -> 0, 1, 2][rotated]
+    NarrowWays() {
+        for (int c = 1; c < kNarrowMaxCols; ++c)
+            for (int vi = 0; vi < 3; ++vi) {
+                const int vec = 1 << vi;
+                if (c % vec) continue;
+                for (int r = 0; r < 2; ++r) ways[c][vi][r] = static_cast<unsigned char>(narrow_bank_ways(c, vec, r != 0));
+            }
+    }
+};
+
 // Shared-memory read width of the narrow kernel.  Rows start every cols
 // words after the tile's staging offset s = (4 - h) % 4, h the floats before
 // the tile's first 16-byte boundary.  Every tile starts a whole number of
@@ -346,29 +412,48 @@ static int narrow_vec(const float* x, int64_t cols) {
     return 1;
 }
 
-bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld) {
-    if (ld != cols || cols <= 0 || cols >= kNarrowMaxCols) return false;
+// How the narrow kernel reads the rows of a (rows, cols) matrix at x, if it
+// takes them at all.
+enum class NarrowRead { kNo, kPlain, kRotated };
+
+static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
+    if (ld != cols || cols <= 0 || cols >= kNarrowMaxCols) return NarrowRead::kNo;
+    const int vec = narrow_vec(x, cols);
     // 16-byte aligned rows of 16, 24, ... columns: the short-row kernel reads
     // them as whole vectors and is faster
-    if (cols % 8 == 0 && cols > 8) return false;
-    // lanes of a warp whose VEC-float reads share banks: gcd(cols/VEC, 32/VEC)
-    const int vec = narrow_vec(x, cols);
-    int64_t a = cols / vec, b = 32 / vec;
-    while (b) { const int64_t r = a % b; a = b; b = r; }
+    if (vec == 4 && cols % 8 == 0 && cols > 8) return NarrowRead::kNo;
+    static const NarrowWays table;
+    const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
     // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
-    return a <= 2 || (cols <= 8 && a <= 4);
+    const int limit = cols <= 8 ? 4 : 2;
+    if (table.ways[cols][vi][0] <= limit) return NarrowRead::kPlain;
+    if (cols / vec <= kRotatedMaxGroups && table.ways[cols][vi][1] <= limit) return NarrowRead::kRotated;
+    return NarrowRead::kNo;
+}
+
+bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld) {
+    return rowsum_narrow_read(x, cols, ld) != NarrowRead::kNo;
 }
 
 cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
-    if (rowsum_use_narrow(x, cols, ld)) {
+    const NarrowRead nr = rowsum_narrow_read(x, cols, ld);
+    if (nr != NarrowRead::kNo) {
         const int64_t rpt = kNarrowTile / cols;  // whole rows per tile
         const int64_t blocks = (rows + rpt - 1) / rpt;
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        const unsigned grid = unsigned(blocks);
+        const bool rot = nr == NarrowRead::kRotated;
         switch (narrow_vec(x, cols)) {
-            case 4: rowsum_narrow_kernel<4><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
-            case 2: rowsum_narrow_kernel<2><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
-            default: rowsum_narrow_kernel<1><<<unsigned(blocks), kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+            case 4: rowsum_narrow_kernel<4, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+            case 2:
+                if (rot) rowsum_narrow_kernel<2, true><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
+                else rowsum_narrow_kernel<2, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
+                break;
+            default:
+                if (rot) rowsum_narrow_kernel<1, true><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
+                else rowsum_narrow_kernel<1, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
+                break;
         }
         return cudaGetLastError();
     }

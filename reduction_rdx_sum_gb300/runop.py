@@ -5,6 +5,7 @@ For quick timings and for profilers (one kernel, a few launches, a chosen size):
     python -m reduction_rdx_sum_gb300.runop --op sum_bf16 --n 268435456 --iters 3
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 262144 --cols 256
     python -m reduction_rdx_sum_gb300.runop --config c5_sum_bf16     # a workload of the suite
+    python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 16777216 --cols 16 --offset 1
 
 Before each timed call the L2 is flushed (a write of 512 MiB, then a read of
 512 MiB so that no dirty line is left for the timed kernel to write back).
@@ -70,7 +71,11 @@ def main(argv=None) -> int:
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--offset", type=int, default=0,
+                    help="start the input this many elements into its allocation (a base off 16-byte alignment)")
     args = ap.parse_args(argv)
+    if args.offset < 0:
+        ap.error("--offset must be >= 0")
     if (args.op is None) == (args.config is None):
         ap.error("give exactly one of --op and --config")
 
@@ -90,6 +95,9 @@ def main(argv=None) -> int:
         args.op = w.op
     else:
         x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
+    if args.offset:
+        buf = torch.empty(x.numel() + args.offset, dtype=x.dtype, device=dev)
+        x = buf[args.offset:].view(x.shape).copy_(x)
     fn = entry(args.op)
     stream = torch.cuda.current_stream(dev)
     flush = None if args.no_flush else L2Flush(dev)

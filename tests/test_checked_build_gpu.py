@@ -114,10 +114,11 @@ def test_row_sums_stay_in_bounds(lib, shape):
     assert violations(lib) == 0
 
 
-@pytest.mark.parametrize("cols", [1, 2, 3, 4, 6, 8, 12, 20, 31, 63])
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 6, 8, 12, 16, 20, 31, 32, 52, 56, 63])
 def test_narrow_row_sums_stay_in_bounds(lib, cols):
     # contiguous rows of fewer than 64 columns: tiles of whole rows staged in
-    # shared memory, at every 4-byte misalignment of the base
+    # shared memory, at every 4-byte misalignment of the base (the rotated
+    # reads of unaligned 8, 12, 16, ... columns included)
     rows = 3 * (4096 // cols) + 5
     host = inputs.uniform_f32(rows * cols, seed=cols, lo=-1.0, hi=1.0).reshape(rows, cols)
     for offset in range(4):

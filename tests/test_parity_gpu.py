@@ -288,12 +288,13 @@ def test_rowsum_narrow_parity(cols, offset):
     assert bad.size == 0, (bad[:5], got[bad[:5]], ref[bad[:5]])
 
 
-@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 8, 12, 31, 63])
-@pytest.mark.parametrize("offset", [0, 1, 2])
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 8, 12, 16, 24, 31, 32, 48, 52, 56, 63])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_rowsum_narrow_exact_integers(cols, offset):
     # small integers: every partial sum is exact in float32, so each row sum
     # must equal the integer sum bit for bit (a misplaced, dropped or doubled
-    # element changes it)
+    # element changes it); the unaligned bases of 8, 12, 16, ... columns take
+    # the rotated reads, whose wrap-around this checks element by element
     rows = 2 * (4096 // cols) + 3
     vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
     x = to_device(vals, offset).view(rows, cols)

@@ -17,3 +17,8 @@ def test_needs_exactly_one_of_op_and_config():
 def test_every_workload_has_an_entry_point():
     for w in inputs.ALL:
         assert callable(runop.entry(w.op))
+
+
+def test_negative_offset_rejected():
+    with pytest.raises(SystemExit):
+        runop.main(["--op", "rowsum_f32", "--offset", "-1"])

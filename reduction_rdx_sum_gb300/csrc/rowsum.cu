@@ -32,7 +32,10 @@ constexpr int kCtaUnroll = 4;    // 16-byte loads in flight per thread, long row
 constexpr int kCtaUnrollDeep = 8;   // the same for rows of kCtaDeepCols or more, at 4 blocks per SM
 constexpr int64_t kCtaDeepCols = 16384;  // measured: deeper is 1 % faster from here, slower below
 constexpr int kGroupBlock = 256; // threads per block, short rows
-constexpr int64_t kGroupRowMaxCols = 5120;  // measured: a block per row is faster from about 6144
+#ifndef RDX_GROUP_ROW_MAX_COLS
+#define RDX_GROUP_ROW_MAX_COLS 5120
+#endif
+constexpr int64_t kGroupRowMaxCols = RDX_GROUP_ROW_MAX_COLS;  // measured: a block per row is faster from about 6144
 constexpr int64_t kFitRowMaxCols = 512;  // 4 vectors x 32 lanes x 4 floats
 #ifndef RDX_ROW_STEPS
 #define RDX_ROW_STEPS 1

@@ -187,8 +187,10 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 #pragma unroll
         for (int u = 0; u < U; ++u) acc[u] = 0.f;
         const size_t span = size_t(cols) * 4;
-        if (t < head && guard(row + t, 4, row, span)) acc[0] += __ldg(row + t);
-        if (t < cols - tail0 && guard(row + tail0 + t, 4, row, span)) acc[U - 1] += __ldg(row + tail0 + t);
+        // the row's up to 3 + 3 edge floats: loaded now, added after the
+        // vectors, so that no vector load waits for their round trip
+        const float eh = t < head && guard(row + t, 4, row, span) ? __ldg(row + t) : 0.f;
+        const float et = t < cols - tail0 && guard(row + tail0 + t, 4, row, span) ? __ldg(row + tail0 + t) : 0.f;
         const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
         int64_t i = t;
         for (; i + (U - 1) * kCtaBlock < m; i += U * kCtaBlock) {
@@ -206,6 +208,8 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
             if (i + u * kCtaBlock < m && guard(rv + i + u * kCtaBlock, 16, row, span))
                 acc[u] += SumF32::fold(ld_stream16(rv + i + u * kCtaBlock));
         }
+        if (t < head) acc[0] += eh;
+        if (t < cols - tail0) acc[U - 1] += et;
         const float a = block_sum<kCtaBlock>(fold_array(acc), smem, 0.f);
         if (t == 0 && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = a;
         __syncthreads();  // smem is reused by the next row

@@ -23,7 +23,7 @@
  *    required.  The output must not overlap the input.
  *  - Scratch: the scalar reductions (and the row sum of few, very long rows)
  *    keep one small workspace per (device, stream) pair (tile partials,
- *    completion counters and, for the exact integer reductions, one
+ *    completion counters and, for the int64 sum and the maxima, one
  *    accumulator word; rdx_workspace_bytes() bytes), allocated by the
  *    library with cudaMalloc on the first call on that pair that needs it and
  *    reused after.  Make that first call outside any CUDA-graph capture, or

@@ -35,7 +35,8 @@ std::map<int, DeviceCaps> g_caps;                          // by device ordinal
 std::map<std::tuple<int, uintptr_t, size_t>, void*> g_workspaces;
 
 // Workspace layout: [completion counters: one per row, kMaxSplitRows of them]
-// [accumulator word of the exact integer reductions, padded to 256 bytes]
+// [accumulator word of the order-independent reductions (int64 sum, maxima),
+//  padded to 256 bytes]
 // [tile partials: reduce_max_partials() slots of 8 bytes].  The counters and
 // the word must be zero before a launch; every launch leaves them zero.
 constexpr size_t kCounterBytes = size_t(rdx::kMaxSplitRows) * sizeof(unsigned);

@@ -87,8 +87,8 @@ struct is_exact<P, decltype(void(P::kExact))> {
     static constexpr bool value = P::kExact;
 };
 
-// Integer reductions whose result has the same bits in any order (int64
-// addition, which is addition modulo 2^64, and the maximum) may finish
+// Reductions whose result has the same bits in any order (int64 addition,
+// which is addition modulo 2^64, and the maxima) may finish
 // through one 8-byte accumulator word per row instead of block partials:
 // every block folds its total in with a fire-and-forget atomic, and the
 // block that draws the last ticket takes the word (reading it and leaving it
@@ -259,6 +259,24 @@ struct MaxF32 {
     __device__ static Acc fold(uint4 v) {
         return Acc(fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                          fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+    }
+    // The word holds the running maximum as an unsigned key that orders as
+    // the floats do: non-negative values with the sign bit set, negative ones
+    // with every bit flipped (-Inf becomes 0x007fffff, -0 sorts just below
+    // +0).  A block total is never NaN (the fold starts from -Inf and fmaxf
+    // drops NaNs), and key 0, which no folded value gives, stands for -Inf.
+    static constexpr bool kWordFinish = true;
+    __device__ static unsigned key(float f) {
+        const unsigned u = __float_as_uint(f);
+        return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    __device__ static void fold_word(unsigned long long* w, Acc a) {
+        atomicMax(w, static_cast<unsigned long long>(key(a.v)));
+    }
+    __device__ static Acc take_word(unsigned long long* w) {
+        const unsigned k = static_cast<unsigned>(atomicExch(w, 0ull));
+        if (k == 0u) return identity();
+        return Acc(__uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k));
     }
 };
 

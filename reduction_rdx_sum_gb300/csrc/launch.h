@@ -48,7 +48,8 @@ size_t reduce_elem_bytes(Op op);
 size_t reduce_acc_bytes(Op op);
 ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols);
 // Whether `op` finishes through an accumulator word instead of partials (the
-// exact integer reductions; rows must then be 1).
+// int64 sum and the maxima, whose result does not depend on the order; rows
+// must then be 1).
 bool reduce_uses_words(Op op);
 // partials: rows * plan.tiles slots (reduce_acc_bytes each; not touched by
 // the word-finishing ops); counters: rows zeroed completion counters, left

@@ -21,10 +21,10 @@
 //   * the tile partials are finished on the device: the block that arrives
 //     last at a completion counter (acquire-release atomic) adds all partials
 //     in a fixed order and resets the counter.  Nothing waits on anything,
-//     and no float atomics are used.  The exact integer reductions (int64
-//     sum, int32 maximum), whose result has the same bits in any order, fold
-//     each block total into one accumulator word with an integer atomic
-//     instead, and the last block only reads that word back.
+//     and no float atomics are used.  The reductions whose result has the
+//     same bits in any order (the int64 sum and both maxima) fold each block
+//     total into one accumulator word with an integer atomic instead, and
+//     the last block only reads that word back.
 // The same kernel sums the rows of a matrix with few, long rows: gridDim.y
 // rows, each cut into tiles with its own completion counter and partials;
 // the scalar reductions are the one-row case.
@@ -134,7 +134,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     }
     unsigned* counter = counters + row;
     if constexpr (has_word_finish<P>::value) {
-        // Exact integer reductions: the block total goes into the row's
+        // Order-independent reductions: the block total goes into the row's
         // accumulator word (a fire-and-forget atomic, released by the ticket
         // that follows it); the block with the last ticket takes the word.
         // One thread does it all: no partial is stored or read again.
@@ -254,7 +254,7 @@ ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     return p;
 }
 
-bool reduce_uses_words(Op op) { return op == Op::SumI32 || op == Op::MaxI32; }
+bool reduce_uses_words(Op op) { return op == Op::SumI32 || op == Op::MaxI32 || op == Op::MaxF32; }
 
 cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
                           void* partials, unsigned* counters, unsigned long long* words, void* out,

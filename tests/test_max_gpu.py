@@ -63,3 +63,33 @@ def test_max_through_workspace_entry():
     z = inputs.integers_i32((1 << 22) + 1, seed=8, lo=-(2 ** 31), hi=2 ** 31 - 1)
     assert abi.rdx_reduce_ws("max_f32", to_device(x), ws).item() == oracle.max_f32(x)
     assert abi.rdx_reduce_ws("max_i32", to_device(z), ws).item() == oracle.max_i32(z)
+
+
+def test_max_word_keys_order_like_floats():
+    # The float maximum finishes through an unsigned key per block total
+    # (non-negative values with the sign bit set, negative ones inverted).
+    # Inputs of many blocks whose maximum is negative, tiny, a zero of either
+    # sign, or -Inf, and maxima that differ from the runner-up in the last bit.
+    n = (1 << 20) + 5
+    cases = {
+        "all negative": np.full(n, -5.0, np.float32),
+        "negative, tiny": np.full(n, -1e-30, np.float32),
+        "zeros of both signs": np.where(np.arange(n) % 2 == 0, np.float32(-0.0), np.float32(0.0)),
+        "only -0": np.full(n, -0.0, np.float32),
+        "only -Inf": np.full(n, -np.inf, np.float32),
+        "subnormals": np.full(n, -1e-44, np.float32),
+    }
+    cases["negative, tiny"][n // 3] = np.float32(-1e-31)
+    cases["subnormals"][n - 7] = np.float32(1e-45)
+    adjacent = np.full(n, np.float32(1.0), np.float32)
+    adjacent[n // 2] = np.nextafter(np.float32(1.0), np.float32(2.0))
+    cases["adjacent floats"] = adjacent
+    nadj = np.full(n, np.float32(-1.0), np.float32)
+    nadj[12345] = np.nextafter(np.float32(-1.0), np.float32(0.0))
+    cases["adjacent negatives"] = nadj
+    for name, x in cases.items():
+        got = abi.rdx_max_f32(to_device(x)).item()
+        assert got == oracle.max_f32(x), name                       # -0 == +0 for a zero maximum
+    # two calls in a row on one stream: the word is left clear for the next
+    assert abi.rdx_max_f32(to_device(cases["all negative"])).item() == -5.0
+    assert abi.rdx_max_f32(to_device(cases["only -Inf"])).item() == -math.inf

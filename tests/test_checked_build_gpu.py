@@ -93,7 +93,8 @@ def test_library_workspace_path_stays_in_bounds(lib):
 
 
 ROWS = [(1, 1, 1), (3, 5, 5), (7, 3, 8), (33, 255, 257), (1000, 256, 256), (100, 256, 300), (64, 1023, 1025),
-        (17, 4099, 4099), (8, 100_000, 100_003), (2, 1 << 20, (1 << 20) + 1), (4, 16384, 16384), (50_000, 7, 7)]
+        (17, 4099, 4099), (8, 100_000, 100_003), (2, 1 << 20, (1 << 20) + 1), (4, 16384, 16384), (50_000, 7, 7),
+        (40, 5121, 5121), (20, 6001, 6007), (2100, 16385, 16385)]
 
 
 @pytest.mark.parametrize("shape", ROWS, ids=str)

@@ -254,7 +254,8 @@ def test_config_rowsum(w):
 
 SHAPES = [(1, 1), (1, 3), (1, 1000), (3, 5), (7, 3), (31, 4), (33, 8), (33, 255), (100, 16), (100, 33),
           (1000, 256), (1000, 257), (513, 64), (64, 1023), (64, 1024), (64, 1025), (17, 2048), (17, 4099),
-          (8, 100_000), (2, 1 << 20), (4097, 128), (50_000, 7), (1, 1 << 22)]
+          (8, 100_000), (2, 1 << 20), (4097, 128), (50_000, 7), (1, 1 << 22),
+          (40, 5121), (300, 6001), (2100, 16385)]   # a block per row, rows of every alignment
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=str)
@@ -302,6 +303,20 @@ def test_rowsum_narrow_exact_integers(cols, offset):
     want = vals.reshape(rows, cols).astype(np.int64).sum(axis=1)
     assert np.array_equal(got.astype(np.int64), want)
     assert np.array_equal(oracle.rowsum_f32(vals.reshape(rows, cols)), want.astype(np.float64))
+
+
+@pytest.mark.parametrize("shape", [(100, 257), (64, 1001), (40, 5121), (300, 6001), (2100, 16385)], ids=str)
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_rowsum_wide_exact_integers(shape, offset):
+    # rows of every alignment through the short-row, warp-per-row and
+    # block-per-row kernels, with small integers whose sums are exact in
+    # float32: each row's head and tail floats must be added exactly once
+    rows, cols = shape
+    vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
+    x = to_device(vals, offset).view(rows, cols)
+    got = abi.rdx_rowsum_f32(x).cpu().numpy()
+    want = vals.reshape(rows, cols).astype(np.int64).sum(axis=1)
+    assert np.array_equal(got.astype(np.int64), want)
 
 
 def test_rowsum_narrow_deterministic_and_matches_strided():

@@ -56,6 +56,15 @@ __device__ __forceinline__ int64_t row_head(const float* row, int64_t cols) {
     return h < cols ? h : cols;
 }
 
+// 4-byte asynchronous copy from global to shared memory (cp.async): the value
+// passes through no register, so nothing waits for it until
+// cp_async_wait_all(), which waits for every copy this thread issued.
+__device__ __forceinline__ void cp_async4(float* smem_dst, const float* src) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Sum of lane l's share of one row, the row split among LPR lanes.
 template <int LPR>
 __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_t cols, int l) {
@@ -116,8 +125,16 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int
 // covers it.  A warp takes units of kRowSteps*NG consecutive rows; in a unit,
 // step q has group g sum row q*NG + g.  All loads of the unit are issued
 // before the first reduction.  Lane 0 of each group stores its row's sum.
+// The up to 3 + 3 floats of a row that is not 16-byte aligned, before its
+// first and after its last whole vector, are copied to shared memory with
+// cp.async ahead of the vector loads (groups of more than two lanes): a
+// load into a register that is added at once would hold the warp for a
+// round trip before its vector loads.  They are added after the vectors, in
+// the same order as before, so the result is the same bit for bit.  Groups
+// of two or more lanes are held to 32 registers (8 blocks per SM); a lane per
+// row needs 37 without spilling.
 template <int LPR>
-__global__ void __launch_bounds__(kGroupBlock)
+__global__ void __launch_bounds__(kGroupBlock, LPR > 1 ? 2048 / kGroupBlock : 1)
 rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                   float* __restrict__ out) {
     constexpr int NG = kWarpSize / LPR;
@@ -128,12 +145,18 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
     const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
     const int64_t nunits = (rows + RU - 1) / RU;
+    constexpr bool kAsyncEdges = LPR > 2;
+    constexpr int kPer = (3 + LPR - 1) / LPR;  // edge floats per lane on each side of a row
+    __shared__ float edge[kRowSteps][2 * kPer][kAsyncEdges ? kGroupBlock : 1];  // [step][head j, tail j][thread]
     for (int64_t k = warp; k < nunits; k += nwarps) {  // one pass unless the grid is capped
         uint4 v[kRowSteps * 4];
-        float sc[kRowSteps];
+        int nh[kRowSteps], nt[kRowSteps];  // head and tail lengths of the step's row (0-3)
+        float sc[kRowSteps];               // without kAsyncEdges: the edge floats' sum
 #pragma unroll
         for (int q = 0; q < kRowSteps; ++q) {
             const int64_t r = k * RU + q * NG + grp;
+            nh[q] = 0;
+            nt[q] = 0;
             sc[q] = 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) v[q * 4 + u] = make_uint4(0u, 0u, 0u, 0u);
@@ -143,10 +166,23 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
                 const int64_t m = (cols - head) >> 2;
                 const int64_t tail0 = head + 4 * m;
                 const size_t span = size_t(cols) * 4;
-                for (int64_t e = l; e < head; e += LPR)
-                    if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
-                for (int64_t e = tail0 + l; e < cols; e += LPR)
-                    if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
+                if (kAsyncEdges) {
+                    nh[q] = int(head);
+                    nt[q] = int(cols - tail0);
+                    for (int e = l; e < nh[q]; e += LPR)
+                        if (guard(row + e, 4, row, span)) cp_async4(&edge[q][e / LPR][threadIdx.x], row + e);
+                    for (int e = l; e < nt[q]; e += LPR)
+                        if (guard(row + tail0 + e, 4, row, span))
+                            cp_async4(&edge[q][kPer + e / LPR][threadIdx.x], row + tail0 + e);
+                } else {
+                    // one or two lanes per row: the copies cost more registers, or
+                    // more time, than the round trip (measured), so the floats are
+                    // added here
+                    for (int64_t e = l; e < head; e += LPR)
+                        if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
+                    for (int64_t e = tail0 + l; e < cols; e += LPR)
+                        if (guard(row + e, 4, row, span)) sc[q] += __ldg(row + e);
+                }
                 const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -156,11 +192,21 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
             }
         }
         batch_fence(v);
+        if (kAsyncEdges) cp_async_wait_all();
 #pragma unroll
         for (int q = 0; q < kRowSteps; ++q) {
             float acc[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) acc[u] = SumF32::fold(v[q * 4 + u]);
+            if (kAsyncEdges) {
+                // the head floats, then the tail floats, in index order
+#pragma unroll
+                for (int j = 0; j < kPer; ++j)
+                    if (l + j * LPR < nh[q]) sc[q] += edge[q][j][threadIdx.x];
+#pragma unroll
+                for (int j = 0; j < kPer; ++j)
+                    if (l + j * LPR < nt[q]) sc[q] += edge[q][kPer + j][threadIdx.x];
+            }
             acc[0] += sc[q];
             float s = group_allreduce<LPR>(fold_array(acc));
             const int64_t r = k * RU + q * NG + grp;

@@ -187,3 +187,37 @@ def test_row_sums_replay_in_a_cuda_graph():
         for host, o in zip(hosts, outs):
             tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
             assert np.all(np.abs(o.cpu().numpy().astype(np.float64) - oracle.rowsum_f32(host)) <= tol)
+
+
+def test_word_finishing_ops_replay_in_a_cuda_graph(workspace):
+    # The int64 sum and the maxima finish through the workspace's accumulator
+    # word, which every launch must leave clear: one graph holding all three,
+    # replayed on new inputs, gives each op's exact result every time.
+    n = (1 << 22) + 3
+    xi = torch.empty(n, dtype=torch.int32, device=DEV)
+    xf = torch.empty(n, device=DEV)
+    outs = [torch.empty((), dtype=torch.int64, device=DEV), torch.empty((), dtype=torch.int32, device=DEV),
+            torch.empty((), device=DEV)]
+    ops = [("sum_i32", xi), ("max_i32", xi), ("max_f32", xf)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        xi.zero_()
+        xf.zero_()
+        for (op, x), out in zip(ops, outs):
+            abi.rdx_reduce_ws(op, x, workspace, out=out, stream=s)   # warm-up
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for (op, x), out in zip(ops, outs):
+            abi.rdx_reduce_ws(op, x, workspace, out=out)
+    for seed in (21, 22, 23):
+        zi = inputs.integers_i32(n, seed, -(2 ** 31), 2 ** 31 - 1)
+        zf = inputs.normal_f32(n, seed)
+        xi.copy_(torch.from_numpy(zi))
+        xf.copy_(torch.from_numpy(zf))
+        g.replay()
+        torch.cuda.synchronize()
+        assert outs[0].item() == oracle.sum_i32(zi)
+        assert outs[1].item() == oracle.max_i32(zi)
+        assert outs[2].item() == oracle.max_f32(zf)

@@ -32,6 +32,12 @@ constexpr int kCtaUnroll = 4;    // 16-byte loads in flight per thread, long row
 constexpr int kCtaUnrollDeep = 8;   // the same for rows of kCtaDeepCols or more, at 4 blocks per SM
 constexpr int64_t kCtaDeepCols = 16384;  // measured: deeper is 1 % faster from here, slower below
 constexpr int kGroupBlock = 256; // threads per block, short rows
+// The warp-per-row kernel's variant for rows that are not 16-byte aligned
+// (edge floats copied with cp.async) needs 43 registers against 32: it wins
+// from about 2048 columns (1 GiB of 4095 columns 153.6 -> 151.6 us, 4096
+// columns 12 bytes off 155.6 -> 151.6 us) and loses below (513 columns
+// 157.7 -> 197 us, 1001 columns 151.6 -> 170 us).
+constexpr int64_t kGroupEdgeMinCols = 2048;
 #ifndef RDX_GROUP_ROW_MAX_COLS
 #define RDX_GROUP_ROW_MAX_COLS 5120
 #endif
@@ -65,9 +71,59 @@ __device__ __forceinline__ void cp_async4(float* smem_dst, const float* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Sum of lane l's share of one row, the row split among LPR lanes.
-template <int LPR>
-__device__ __forceinline__ float row_share(const float* __restrict__ row, int64_t cols, int l) {
+// Sum of lane l's share of one row, the row split among LPR lanes.  With
+// EDGES (the matrix has rows that are not 16-byte aligned) the up to 3 + 3
+// floats before the first and after the last whole vector are copied with
+// cp.async to the thread's slots edge[0], edge[stride], ... ahead of the
+// vector loads and added to acc[0] and acc[1] just before the first vector
+// is: the same additions in the same order as adding them on arrival
+// (without EDGES), without holding the warp for their round trip first.
+template <int LPR, bool EDGES>
+__device__ __forceinline__ float row_share(const float* __restrict__ row, int64_t cols, int l, float* edge,
+                                           int stride) {
+    if (EDGES) {
+        constexpr int kPer = (3 + LPR - 1) / LPR;
+        const int64_t head = row_head(row, cols);
+        const int64_t m = (cols - head) >> 2;
+        const int64_t tail0 = head + 4 * m;
+        const int nh = int(head), nt = int(cols - tail0);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const size_t span = size_t(cols) * 4;
+        for (int e = l; e < nh; e += LPR)
+            if (guard(row + e, 4, row, span)) cp_async4(edge + (e / LPR) * stride, row + e);
+        for (int e = l; e < nt; e += LPR)
+            if (guard(row + tail0 + e, 4, row, span)) cp_async4(edge + (kPer + e / LPR) * stride, row + tail0 + e);
+        bool pending = true;
+        auto add_edges = [&]() {
+            cp_async_wait_all();
+#pragma unroll
+            for (int k = 0; k < kPer; ++k)
+                if (l + k * LPR < nh) acc[0] += edge[k * stride];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k)
+                if (l + k * LPR < nt) acc[1] += edge[(kPer + k) * stride];
+            pending = false;
+        };
+        const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
+        int64_t j = l;
+        for (; j + 3 * LPR < m; j += 4 * LPR) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = guard(rv + j + u * LPR, 16, row, span) ? ld_stream16(rv + j + u * LPR) : SumF32::neutral();
+            batch_fence(v);
+            if (pending) add_edges();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] += SumF32::fold(v[u]);
+        }
+        if (pending) add_edges();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (j + u * LPR < m && guard(rv + j + u * LPR, 16, row, span))
+                acc[u] += SumF32::fold(ld_stream16(rv + j + u * LPR));
+        }
+        return fold_array(acc);
+    }
     const int64_t head = row_head(row, cols);
     const int64_t m = (cols - head) >> 2;
     const int64_t tail0 = head + 4 * m;
@@ -101,7 +157,7 @@ __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_
 // Short rows.  Group g of warp w (lanes g*LPR .. g*LPR+LPR-1) sums row
 // (w + k * nwarps) * NG + g for k = 0, 1, ...; lane 0 of the group stores it.
 // The NG rows of one warp step are consecutive, so are their sums.
-template <int LPR>
+template <int LPR, bool EDGES>
 __global__ void __launch_bounds__(kGroupBlock)
 rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                     float* __restrict__ out) {
@@ -112,10 +168,12 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int
     const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
     const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
     const int64_t nsteps = (rows + NG - 1) / NG;
+    constexpr int kPer = (3 + LPR - 1) / LPR;
+    __shared__ float edge[EDGES ? 2 * kPer : 1][EDGES ? kGroupBlock : 1];  // the rows' edge floats
     for (int64_t k = warp; k < nsteps; k += nwarps) {
         const int64_t r = k * NG + grp;
         float s = 0.f;
-        if (r < rows) s = row_share<LPR>(x + r * ld, cols, l);
+        if (r < rows) s = row_share<LPR, EDGES>(x + r * ld, cols, l, &edge[0][EDGES ? threadIdx.x : 0], kGroupBlock);
         s = group_allreduce<LPR>(s);  // every lane takes part, in range or not
         if (l == 0 && r < rows && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = s;
     }
@@ -398,7 +456,7 @@ cudaError_t launch_fit(const float* x, int64_t rows, int64_t cols, int64_t ld, f
     return cudaGetLastError();
 }
 
-template <int LPR>
+template <int LPR, bool EDGES>
 cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     constexpr int64_t kNG = kWarpSize / LPR;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
@@ -406,7 +464,7 @@ cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld,
     int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     // one step per warp, as in launch_fit
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
-    rowsum_group_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
+    rowsum_group_kernel<LPR, EDGES><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
     return cudaGetLastError();
 }
 
@@ -520,7 +578,14 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
             default: return launch_fit<32>(x, rows, cols, ld, out, stream);
         }
     }
-    if (cols <= kGroupRowMaxCols) return launch_group<32>(x, rows, cols, ld, out, stream);
+    if (cols <= kGroupRowMaxCols) {
+        // rows that are not all 16-byte aligned and at least kGroupEdgeMinCols
+        // long take the variant that copies their edge floats
+        const bool edges =
+            cols >= kGroupEdgeMinCols && (reinterpret_cast<uintptr_t>(x) % 16 != 0 || ld % 4 != 0);
+        return edges ? launch_group<32, true>(x, rows, cols, ld, out, stream)
+                     : launch_group<32, false>(x, rows, cols, ld, out, stream);
+    }
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
     if (cols >= kCtaDeepCols)
         rowsum_cta_kernel<kCtaUnrollDeep, 4><<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);

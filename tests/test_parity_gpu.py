@@ -305,7 +305,8 @@ def test_rowsum_narrow_exact_integers(cols, offset):
     assert np.array_equal(oracle.rowsum_f32(vals.reshape(rows, cols)), want.astype(np.float64))
 
 
-@pytest.mark.parametrize("shape", [(100, 257), (64, 1001), (40, 5121), (300, 6001), (2100, 16385)], ids=str)
+@pytest.mark.parametrize("shape", [(100, 257), (64, 1001), (20, 2049), (12, 4095), (40, 5121), (300, 6001),
+                                   (2100, 16385)], ids=str)
 @pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_rowsum_wide_exact_integers(shape, offset):
     # rows of every alignment through the short-row, warp-per-row and

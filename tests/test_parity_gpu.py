@@ -157,6 +157,21 @@ def test_integer_accumulator_word_left_clear_between_ops():
         assert got.item() == oracle.max_i32(hosts[rep])
 
 
+def test_subnormal_inputs_are_not_flushed():
+    # n copies of the smallest subnormal: every partial sum is a multiple of
+    # it well inside float32's exact range, so the sum is exactly n times it
+    # in any order (a build that flushed subnormals to zero would return 0)
+    n = (1 << 20) + 3
+    tiny = np.float32(2.0 ** -149)                      # smallest float32 subnormal
+    x = np.full(n, tiny, np.float32)
+    assert abi.rdx_sum_f32(to_device(x, 1)).item() == n * 2.0 ** -149 == oracle.sum_f32(x)
+    rows = x[: 1000 * 1000].reshape(1000, 1000)
+    assert np.all(abi.rdx_rowsum_f32(to_device(rows.reshape(-1)).view(1000, 1000)).cpu().numpy() == np.float32(1000 * 2.0 ** -149))
+    b = np.full(n, 0x0001, np.uint16)                    # smallest bfloat16 subnormal, 2^-133
+    assert abi.rdx_sum_bf16_f32acc(to_device(b, 3)).item() == n * 2.0 ** -133 == oracle.sum_bf16(b)
+    assert abi.rdx_max_f32(to_device(x)).item() == 2.0 ** -149
+
+
 def test_nonfinite_propagation():
     n = 100_003
     for pos in (0, 5, n // 2, n - 1):

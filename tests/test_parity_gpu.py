@@ -172,6 +172,19 @@ def test_subnormal_inputs_are_not_flushed():
     assert abi.rdx_max_f32(to_device(x)).item() == 2.0 ** -149
 
 
+def test_overflow_gives_infinity():
+    # same-sign terms whose exact sum passes the largest float32: the float32
+    # result, correctly rounded, is the infinity of their sign, whatever the
+    # order of the additions
+    n = (1 << 20) + 1
+    x = np.full(n, np.float32(1e33), np.float32)        # exact sum 1.05e39 > 3.4e38
+    assert abi.rdx_sum_f32(to_device(x)).item() == math.inf
+    assert abi.rdx_sum_f32(to_device(-x)).item() == -math.inf
+    assert abi.rdx_sumsq_f32(to_device(np.full(n, np.float32(1e17), np.float32))).item() == math.inf
+    rows = np.full(4 * 65536, np.float32(1e34), np.float32)  # each row's exact sum 6.6e38
+    assert abi.rdx_rowsum_f32(to_device(rows).view(4, 65536)).tolist() == [math.inf] * 4
+
+
 def test_nonfinite_propagation():
     n = 100_003
     for pos in (0, 5, n // 2, n - 1):

@@ -59,6 +59,16 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization (launch_pdl) may be scheduled while the kernel ahead of it in
+// the stream is still running.  pdl_wait() holds the thread until that kernel
+// has completed and its memory writes are visible (for a kernel launched
+// without the attribute it returns at once), so it comes before the first
+// global memory access.  pdl_release() lets the next such kernel be scheduled
+// onto the SMs this grid leaves free; it waits there in pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Issue order fence for a batch of loads: every register of v passes through
 // an empty volatile asm placed after the whole batch, so no arithmetic on the
 // batch can be scheduled between its loads and all N loads are in flight

@@ -8,6 +8,24 @@
 
 namespace rdx {
 
+// Launch `kernel` with programmatic stream serialization: it may start while
+// the kernel ahead of it in the stream drains, and waits in pdl_wait() until
+// that kernel's writes are visible (see device.cuh).
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // The scalar reductions of the C ABI, numbered as the RDX_OP_* codes
 // (SumSumSq*: sum and sum of squares in one pass).
 enum class Op : int {

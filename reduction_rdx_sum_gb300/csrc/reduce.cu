@@ -77,6 +77,8 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     constexpr int V = P::kVec;
     __shared__ Acc smem[kBlock / kWarpSize];
     __shared__ unsigned last_block;
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
 
     // This block's row and tile.  head = elements before the row's first
     // 16-byte boundary, then m whole 16-byte vectors, then the tail.
@@ -201,12 +203,10 @@ cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, 
     auto* pt = static_cast<typename P::Acc*>(partials);
     auto* ot = static_cast<typename P::Acc*>(out);
     if (plan.large)
-        reduce_kernel<P, kUnrollLarge, kMinBlocksLarge><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
-                                                                                     counters, words, ot);
-    else
-        reduce_kernel<P, kUnroll, kMinBlocksPerSm><<<grid, kBlock, 0, stream>>>(xt, cols, ld, plan.tile, pt,
-                                                                                counters, words, ot);
-    return cudaGetLastError();
+        return launch_pdl(reduce_kernel<P, kUnrollLarge, kMinBlocksLarge>, grid, dim3(kBlock), stream, xt, cols, ld,
+                          plan.tile, pt, counters, words, ot);
+    return launch_pdl(reduce_kernel<P, kUnroll, kMinBlocksPerSm>, grid, dim3(kBlock), stream, xt, cols, ld, plan.tile,
+                      pt, counters, words, ot);
 }
 
 }  // namespace

@@ -161,6 +161,8 @@ template <int LPR, bool EDGES>
 __global__ void __launch_bounds__(kGroupBlock)
 rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                     float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
     constexpr int NG = kWarpSize / LPR;  // rows in flight per warp step
     const int lane = threadIdx.x % kWarpSize;
     const int grp = lane / LPR;
@@ -195,6 +197,8 @@ template <int LPR>
 __global__ void __launch_bounds__(kGroupBlock, LPR > 1 ? 2048 / kGroupBlock : 1)
 rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                   float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
     constexpr int NG = kWarpSize / LPR;
     constexpr int RU = NG * kRowSteps;  // rows per unit
     const int lane = threadIdx.x % kWarpSize;
@@ -280,6 +284,8 @@ rowsum_fit_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 template <int U, int kMinBlocks>
 __global__ void __launch_bounds__(kCtaBlock, kMinBlocks)
 rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
     __shared__ float smem[kCtaBlock / kWarpSize];
     const int t = threadIdx.x;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -346,6 +352,8 @@ template <int VEC, bool ROT>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
                      float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
     __shared__ __align__(16) float tile[kNarrowTile + 4];
     const int t = threadIdx.x;
     const int ci = int(cols);
@@ -452,8 +460,7 @@ cudaError_t launch_fit(const float* x, int64_t rows, int64_t cols, int64_t ld, f
     // they free up (measured faster than a capped grid looping over units)
     int64_t blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
-    rowsum_fit_kernel<LPR><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
-    return cudaGetLastError();
+    return launch_pdl(rowsum_fit_kernel<LPR>, dim3(unsigned(blocks)), dim3(kGroupBlock), stream, x, rows, cols, ld, out);
 }
 
 template <int LPR, bool EDGES>
@@ -464,8 +471,8 @@ cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld,
     int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     // one step per warp, as in launch_fit
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
-    rowsum_group_kernel<LPR, EDGES><<<unsigned(blocks), kGroupBlock, 0, stream>>>(x, rows, cols, ld, out);
-    return cudaGetLastError();
+    return launch_pdl(rowsum_group_kernel<LPR, EDGES>, dim3(unsigned(blocks)), dim3(kGroupBlock), stream, x, rows, cols,
+                      ld, out);
 }
 
 }  // namespace
@@ -553,20 +560,17 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
         const int64_t rpt = kNarrowTile / cols;  // whole rows per tile
         const int64_t blocks = (rows + rpt - 1) / rpt;
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        const unsigned grid = unsigned(blocks);
+        const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
         const bool rot = nr == NarrowRead::kRotated;
         switch (narrow_vec(x, cols)) {
-            case 4: rowsum_narrow_kernel<4, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out); break;
+            case 4: return launch_pdl(rowsum_narrow_kernel<4, false>, grid, block, stream, x, rows, cols, rpt, out);
             case 2:
-                if (rot) rowsum_narrow_kernel<2, true><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
-                else rowsum_narrow_kernel<2, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
-                break;
+                return rot ? launch_pdl(rowsum_narrow_kernel<2, true>, grid, block, stream, x, rows, cols, rpt, out)
+                           : launch_pdl(rowsum_narrow_kernel<2, false>, grid, block, stream, x, rows, cols, rpt, out);
             default:
-                if (rot) rowsum_narrow_kernel<1, true><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
-                else rowsum_narrow_kernel<1, false><<<grid, kNarrowBlock, 0, stream>>>(x, rows, cols, rpt, out);
-                break;
+                return rot ? launch_pdl(rowsum_narrow_kernel<1, true>, grid, block, stream, x, rows, cols, rpt, out)
+                           : launch_pdl(rowsum_narrow_kernel<1, false>, grid, block, stream, x, rows, cols, rpt, out);
         }
-        return cudaGetLastError();
     }
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {
@@ -588,10 +592,10 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
     }
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
     if (cols >= kCtaDeepCols)
-        rowsum_cta_kernel<kCtaUnrollDeep, 4><<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
-    else
-        rowsum_cta_kernel<kCtaUnroll, 8><<<unsigned(blocks), kCtaBlock, 0, stream>>>(x, rows, cols, ld, out);
-    return cudaGetLastError();
+        return launch_pdl(rowsum_cta_kernel<kCtaUnrollDeep, 4>, dim3(unsigned(blocks)), dim3(kCtaBlock), stream, x, rows,
+                          cols, ld, out);
+    return launch_pdl(rowsum_cta_kernel<kCtaUnroll, 8>, dim3(unsigned(blocks)), dim3(kCtaBlock), stream, x, rows, cols, ld,
+                      out);
 }
 
 }  // namespace rdx

@@ -54,21 +54,21 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "13bb630071ea000b"
-_ROW_HASH = "8e59e8f27c6960c2"
+_RED_HASH = "a6f536c6cc94ecd4"
+_ROW_HASH = "fda490a938249909"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2158973966, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2160056334, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2158709774, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2159155214, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1078760960, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1079200768, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67254272, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67259648, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_8192x32768": {"bytes_per_launch": 1079388672, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_8192x32768": {"bytes_per_launch": 1080155136, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086098432, "sources": _ROW, "source_hash": _ROW_HASH,
+    "c4_rowsum_1048576x256": {"bytes_per_launch": 1086040064, "sources": _ROW, "source_hash": _ROW_HASH,
                               "profile": "profiles/kernels_dram_traffic_small_cases.md"},
 }
 

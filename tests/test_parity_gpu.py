@@ -475,6 +475,31 @@ def test_rowsum_deterministic():
             assert torch.equal(abi.rdx_rowsum_f32(x).view(torch.int32), a.view(torch.int32))
 
 
+def test_chained_calls_read_each_others_results():
+    # Each call below reads what the call before it wrote, queued back to back
+    # on one stream with no host synchronisation: a kernel launched behind
+    # another may start early (programmatic dependent launch) and must still
+    # see every write of the one ahead.  Small integers keep every result
+    # exact, so any stale read shows.
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for seed in range(20):
+            host = (np.random.default_rng(seed).integers(-3, 4, size=(1024, 512))).astype(np.float32)
+            x = torch.from_numpy(host).to(DEV, non_blocking=False)
+            r = abi.rdx_rowsum_f32(x, stream=s)                       # 1024 row sums
+            t = abi.rdx_sum_f32(r, stream=s)                          # their total
+            m = abi.rdx_max_f32(r, stream=s)                          # their maximum
+            rr = abi.rdx_rowsum_f32(r.view(16, 64), stream=s)          # sums of 64 row sums
+            t2 = abi.rdx_sum_f32(rr, stream=s)                        # the total again
+            z = abi.rdx_sum_i32_i64(r.to(torch.int32), stream=s)     # through a torch kernel
+            s.synchronize()
+            rows = host.astype(np.int64).sum(axis=1)
+            assert np.array_equal(r.cpu().numpy().astype(np.int64), rows)
+            assert t.item() == t2.item() == z.item() == rows.sum()
+            assert m.item() == rows.max()
+            assert np.array_equal(rr.cpu().numpy().astype(np.int64), rows.reshape(16, 64).sum(axis=1))
+
+
 def test_concurrent_streams():
     hosts = [inputs.normal_f32((1 << 22) + i, seed=10 + i) for i in range(4)]
     devs = [torch.from_numpy(h).to(DEV) for h in hosts]

@@ -1,0 +1,79 @@
+"""Seeded random shapes against the oracle: row sums over every kernel
+choice (narrow plain and rotated, short rows, a warp per row, a block per
+row, split rows; contiguous and with a leading dimension; every 4-byte base
+offset), and scalar reductions over sizes and offsets around every tiling
+threshold.  Each case is small; the seeds make every run the same."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from reduction_rdx_sum_gb300 import abi, inputs
+
+from test_parity_gpu import DEV, VEC, check, host_input, to_device
+
+pytestmark = pytest.mark.gpu
+
+MAX_ELEMS = 1 << 22  # per case
+
+
+def _row_shape(rng):
+    cols = int(math.exp(rng.uniform(0.0, math.log(40000.0))))
+    cols = max(cols, 1)
+    rows = int(math.exp(rng.uniform(0.0, math.log(5000.0))))
+    rows = max(1, min(rows, MAX_ELEMS // (cols + 17)))
+    ld = cols if rng.random() < 0.6 else cols + int(rng.integers(1, 18))
+    offset = int(rng.integers(0, 4))
+    return rows, cols, ld, offset
+
+
+@pytest.mark.parametrize("case", range(120))
+def test_random_row_shapes(case):
+    rng = np.random.default_rng(1000 + case)
+    rows, cols, ld, offset = _row_shape(rng)
+    exact = case % 3 == 0
+    if exact:   # small integers: every row sum exact in float32
+        full = (rng.integers(-7, 8, size=rows * ld)).astype(np.float32)
+    else:
+        full = inputs.uniform_f32(rows * ld, seed=case, lo=-1.0, hi=1.0)
+    buf = torch.empty(rows * ld + offset, dtype=torch.float32, device=DEV)
+    buf[offset:].copy_(torch.from_numpy(full))
+    x = buf[offset:].view(rows, ld)[:, :cols]
+    got = (abi.rdx_rowsum_f32(x) if ld == cols else abi.rdx_rowsum_strided_f32(x)).cpu().numpy()
+    host = np.ascontiguousarray(full.reshape(rows, ld)[:, :cols])
+    if exact:
+        assert np.array_equal(got.astype(np.int64), host.astype(np.int64).sum(axis=1)), (rows, cols, ld, offset)
+    else:
+        ref = oracle.rowsum_f32(host)
+        tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+        bad = np.nonzero(~(np.abs(got.astype(np.float64) - ref) <= tol))[0]
+        assert bad.size == 0, (rows, cols, ld, offset, bad[:5])
+
+
+OPS = ["sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32"]
+
+
+@pytest.mark.parametrize("case", range(120))
+def test_random_scalar_sizes(case):
+    rng = np.random.default_rng(5000 + case)
+    op = OPS[case % len(OPS)]
+    n = int(math.exp(rng.uniform(0.0, math.log(float(1 << 24)))))
+    offset = int(rng.integers(0, VEC[op]))
+    host = host_input(op, n, seed=case)
+    x = to_device(host, offset)
+    got = abi.SCALAR_OPS[op](x).item()
+    check(op, host, got)
+    assert abi.SCALAR_OPS[op](x).item() == got  # the same bits again
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_maxima(case):
+    rng = np.random.default_rng(9000 + case)
+    n = int(math.exp(rng.uniform(0.0, math.log(float(1 << 23)))))
+    offset = int(rng.integers(0, 4))
+    f = inputs.normal_f32(n, seed=case) * np.float32(rng.choice([1e-40, 1.0, 1e30]))
+    z = inputs.integers_i32(n, seed=case, lo=-(2 ** 31), hi=2 ** 31 - 1)
+    assert abi.rdx_max_f32(to_device(f, offset)).item() == oracle.max_f32(f)
+    assert abi.rdx_max_i32(to_device(z, offset)).item() == oracle.max_i32(z)

@@ -25,6 +25,9 @@
 //     same bits in any order (the int64 sum and both maxima) fold each block
 //     total into one accumulator word with an integer atomic instead, and
 //     the last block only reads that word back.
+// Launched with programmatic dependent launch, a call queued behind another
+// kernel is scheduled while that kernel drains and starts reading once its
+// writes are visible.
 // The same kernel sums the rows of a matrix with few, long rows: gridDim.y
 // rows, each cut into tiles with its own completion counter and partials;
 // the scalar reductions are the one-row case.

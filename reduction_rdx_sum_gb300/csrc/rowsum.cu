@@ -16,9 +16,14 @@
 //   * long rows: one block per row, the same add-on-load loop and block tree
 //     as the scalar reduction (twice the loads in flight at half the
 //     occupancy from kCtaDeepCols columns), a direct store of the row's sum.
-// Rows may start every ld >= cols elements (a leading dimension).  A row's
-// summation order depends only on the shape and the alignment of x, never on
-// the grid or the device, so the result is bitwise reproducible.  No
+// Rows may start every ld >= cols elements (a leading dimension).  Rows that
+// are not 16-byte aligned have up to 3 floats before their first and after
+// their last whole vector: the narrow kernel reads such rows from shared
+// memory in a rotated order, the others fetch those edge floats without
+// holding the row's vector loads back (cp.async copies, or registers loaded
+// ahead).  Every kernel is launched with programmatic dependent launch.  A
+// row's summation order depends only on the shape and the alignment of x,
+// never on the grid or the device, so the result is bitwise reproducible.  No
 // workspace is needed.  (Few, very long rows go to the tiled kernel of
 // reduce.cu instead; see rowsum_use_split.)
 #include "device.cuh"

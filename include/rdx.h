@@ -97,30 +97,55 @@ rdx_status rdx_sum_f32(const float* x, int64_t n, float* out, cudaStream_t strea
 
 /*
  * rdx_sumsq_f32: *out = sum_{i<n} x[i]^2, float32 accumulation.
- * The same reduction with the square of each input as the term (the
- * "one add per element" of the page becomes one multiply-add per element).
+ * Page "03_shared_memory_sync_reduction.py", demo 3's sum with the square of
+ * each input as the term: the page's one add per element becomes one
+ * multiply-add.  The pages give no sum of squares of their own; it is one of
+ * this library's five named operations, run on the 2^24 + 13-element
+ * normal(0, 1) float32 workload beside its plain sum.  The result is within
+ * 1e-6 * sum x_i^2 of the exact sum of squares.
  * Arguments and errors as rdx_sum_f32.
  */
 rdx_status rdx_sumsq_f32(const float* x, int64_t n, float* out, cudaStream_t stream);
 
 /*
  * rdx_sum_bf16_f32acc: *out = sum_{i<n} x[i], bfloat16 input widened exactly
- * to float32, float32 accumulation.  x is 2-byte aligned.
+ * to float32, float32 accumulation.
+ * Page "03_shared_memory_sync_reduction.py", demo 3's sum over a 2-byte
+ * element: half the bytes per add of the page's float32 input (the pages'
+ * simulator holds 4-byte types only: page "simt_lab.py", section 3, shared
+ * arrays).  One of this library's
+ * five named operations, run on the 2^30 + 7-element workload of normal(0, 1)
+ * values rounded to bfloat16.  The result is within 4e-6 * sum |x_i| of the
+ * exact sum.  x is 2-byte aligned.
  * Arguments and errors as rdx_sum_f32.
  */
 rdx_status rdx_sum_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaStream_t stream);
 
 /*
  * rdx_sumsq_bf16_f32acc: *out = sum_{i<n} x[i]^2, bfloat16 input, float32
- * accumulation.  Arguments and errors as rdx_sum_bf16_f32acc.
+ * accumulation: rdx_sumsq_f32's term over rdx_sum_bf16_f32acc's input.  The
+ * 2^30 + 7-element bfloat16 workload asks for its sum of squares beside its
+ * sum; the five named operations have no bfloat16 sum of squares, so this
+ * sixth one is exported with the same signature.  The result is within
+ * 4e-6 * sum x_i^2 of the exact sum of squares.
+ * Arguments and errors as rdx_sum_bf16_f32acc.
  */
 rdx_status rdx_sumsq_bf16_f32acc(const rdx_bf16* x, int64_t n, float* out, cudaStream_t stream);
 
 /*
  * rdx_sum_i32_i64: *out = sum_{i<n} x[i], int32 input, int64 accumulation.
- * Integer addition is associative, so the result is exact and equal to the
- * sequential sum bit for bit (no overflow for n < 2^32).  x 4-byte aligned,
- * out 8-byte aligned.  Other arguments and errors as rdx_sum_f32.
+ * Page "03_shared_memory_sync_reduction.py", demo 3's sum over int32 values
+ * (the simulator's shared arrays hold float32 and int32 alike: page
+ * "simt_lab.py", section 3), widened to int64 so that it cannot overflow in
+ * practice.  One of this library's five named
+ * operations, run on the 2^28-element workload of uniform integers in
+ * [-2^20, 2^20] and required bit-exact.
+ * The accumulation is int64 addition, i.e. addition modulo 2^64 of the
+ * values' two's-complement bits: it is associative, so the result is the
+ * sequential sum bit for bit in any grouping.  It equals the mathematical sum
+ * whenever |sum| < 2^63, which every n < 2^32 guarantees (|x_i| <= 2^31);
+ * beyond that the result wraps modulo 2^64 (no error is raised).  x 4-byte
+ * aligned, out 8-byte aligned.  Other arguments and errors as rdx_sum_f32.
  */
 rdx_status rdx_sum_i32_i64(const int32_t* x, int64_t n, int64_t* out, cudaStream_t stream);
 

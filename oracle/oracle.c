@@ -14,7 +14,7 @@
  *   - floating-point sums here are float64 with Kahan compensation
  *     (y = x - c; t = s + y; c = (t - s) - y; s = t), so the oracle is far
  *     more accurate than any float32 GPU result it is compared with;
- *   - integer sums are plain int64 accumulation, exact for any n < 2^32;
+ *   - integer sums are int64 accumulation modulo 2^64, exact for any n < 2^32;
  *   - the row-segmented sum is the same loop run once per row.  On the page,
  *     versions 1-3 write one partial per block of B consecutive inputs and
  *     versions 4-5 one per 2B, so a block's output is a segment sum; a row
@@ -122,11 +122,20 @@ double oracle_abssum_bf16(const uint16_t* x, int64_t n) {
 
 /* ---- int32 input, int64 result ----------------------------------------- */
 
-/* Exact: |x_i| <= 2^31, so any n < 2^32 keeps |sum| < 2^63. */
+/* The int64 sum of int32 values, defined as addition modulo 2^64 (the
+ * two's-complement int64 the result is returned in).  Exact, and equal to the
+ * mathematical sum, while |sum| < 2^63, which any n < 2^32 guarantees
+ * (|x_i| <= 2^31).  The loop adds in uint64_t, whose wrap-around C defines,
+ * so a sum past 2^63 wraps instead of being signed overflow. */
+static int64_t from_twos_complement(uint64_t u) {
+    if (u <= (uint64_t)INT64_MAX) return (int64_t)u;
+    return -(int64_t)(~u) - 1; /* u - 2^64, without overflow */
+}
+
 int64_t oracle_sum_i32(const int32_t* x, int64_t n) {
-    int64_t s = 0;
-    for (int64_t i = 0; i < n; ++i) s += (int64_t)x[i];
-    return s;
+    uint64_t s = 0;
+    for (int64_t i = 0; i < n; ++i) s += (uint64_t)(int64_t)x[i];
+    return from_twos_complement(s);
 }
 
 /* ---- row-segmented float32 sum (row-major, contiguous) ----------------- */

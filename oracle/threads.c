@@ -103,13 +103,13 @@ int oracle_threaded_reduce(int op, const void* x, int64_t n, int threads, double
     const int k = split(op, x, n, threads, 0, NULL, cs);
     if (run_all(cs, k) != 0) return -1;
     double d = 0.0;
-    int64_t i = 0;
+    uint64_t i = 0; /* modulo 2^64, as the single-thread loop */
     for (int t = 0; t < k; ++t) {
         d += cs[t].d;
-        i += cs[t].i;
+        i += (uint64_t)cs[t].i;
     }
     if (out_d) *out_d = d;
-    if (out_i) *out_i = i;
+    if (out_i) *out_i = i <= (uint64_t)INT64_MAX ? (int64_t)i : -(int64_t)(~i) - 1;
     return 0;
 }
 

@@ -29,8 +29,8 @@ C_MUTANTS = [
     ("square without the square", "        double v = (double)x[i];\n        kahan_add(&k, v * v);",
      "        double v = (double)x[i];\n        kahan_add(&k, v * fabs(v));"),
     ("bf16 widened by 15 bits", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
-    ("int sum in 32 bits", "for (int64_t i = 0; i < n; ++i) s += (int64_t)x[i];",
-     "for (int64_t i = 0; i < n; ++i) s = (int32_t)(s + x[i]);"),
+    ("int sum in 32 bits", "for (int64_t i = 0; i < n; ++i) s += (uint64_t)(int64_t)x[i];",
+     "for (int64_t i = 0; i < n; ++i) s = (uint32_t)(s + (uint64_t)(int64_t)x[i]);"),
     ("row stride off by one", "const float* row = x + r * cols;\n        kahan_acc k;\n        kahan_init(&k);\n        for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);",
      "const float* row = x + r * (cols + (r > 0));\n        kahan_acc k;\n        kahan_init(&k);\n        for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);"),
     ("rows summed as columns", "for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);\n        out[r] = kahan_result(&k);",

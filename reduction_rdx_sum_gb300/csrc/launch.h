@@ -50,6 +50,13 @@ struct DeviceCaps {
 };
 
 // ---- tiled reductions (reduce.cu) -----------------------------------------
+// Most tiles (= block partials) one call of the tiled reductions uses, over
+// all its rows: the size of every partials buffer (the library's workspace,
+// a caller's workspace, the static scratch of the no-allocation sum).
+#ifndef RDX_REDUCE_MAX_TILES
+#define RDX_REDUCE_MAX_TILES 8192
+#endif
+constexpr int64_t kReduceMaxTiles = RDX_REDUCE_MAX_TILES;
 // One call sums `rows` segments of `cols` elements, segment r starting at
 // x + r * ld (the scalar reductions: rows = 1).  Each row is cut into `tiles`
 // tiles of `tile` 16-byte vectors, one block each; the plan depends only on

@@ -35,7 +35,9 @@
 
 namespace {
 
-constexpr int kMaxPartials = 8192;  // block partials the scratch holds
+// block partials the scratch holds: as many as any call of the tiled
+// reductions uses, so the limit follows a build that changes the tiling
+constexpr int64_t kMaxPartials = rdx::kReduceMaxTiles;
 constexpr size_t kCounterBytes = 256;
 constexpr size_t kScratchBytes = kCounterBytes + size_t(kMaxPartials) * sizeof(float);
 

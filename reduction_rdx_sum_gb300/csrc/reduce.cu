@@ -40,9 +40,6 @@
 #ifndef RDX_REDUCE_BLOCK
 #define RDX_REDUCE_BLOCK 256
 #endif
-#ifndef RDX_REDUCE_MAX_TILES
-#define RDX_REDUCE_MAX_TILES 8192
-#endif
 #ifndef RDX_REDUCE_MIN_TILE
 #define RDX_REDUCE_MIN_TILE 1024
 #endif
@@ -53,7 +50,7 @@ namespace {
 constexpr int kBlock = RDX_REDUCE_BLOCK;                  // threads per block
 constexpr int kUnroll = 4;                                // 16-byte loads in flight per thread
 constexpr int kUnrollLarge = 8;                           // the same, inputs of kLargeTiles tiles or more
-constexpr int64_t kMaxTiles = RDX_REDUCE_MAX_TILES;       // tiles (= partials) aimed at per call
+constexpr int64_t kMaxTiles = kReduceMaxTiles;            // tiles (= partials) aimed at per call
 constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per tile, at least
 constexpr int64_t kMidTiles = 1024;                       // tiles aimed at for mid-size inputs
 constexpr int64_t kMidTileCap = 4096;                     // largest tile of the mid-size rule (64 KiB)

@@ -1,7 +1,18 @@
-"""rdx_sum_f32_noalloc: the float32 sum that allocates no device memory (for
-callers inside a framework that owns all device memory, latency-critical
-callers, and fixed-budget programs).  Checked against rdx_sum_f32, through the
-C ABI, on two calls in a row that share the library's static scratch.
+"""rdx_sum_f32_noalloc: the float32 sum that allocates no device memory.
+
+Some callers of this library may not call cudaMalloc while they run: code
+inside a framework whose caching allocator owns all device memory, latency-
+critical code for which cudaMalloc/cudaFree can synchronize the device, and
+programs whose memory budget is fixed at start-up.  This entry point serves
+them with scratch held in one static device array of the library.
+
+It runs the kernel, grid and summation order of rdx_sum_f32, so its result
+must be bitwise identical to rdx_sum_f32's, and within the float32 tolerance
+of the oracle.  Every case is called twice in a row through the C ABI (the
+second call reuses the scratch the first one left), on a stream of its own
+and on the default stream, at 16-byte-aligned and misaligned bases; one case
+(2^28 elements, 1 GiB) needs exactly the 8192 block partials the static
+scratch holds.
 
 This file is collected last on purpose: it must pass both alone in a fresh
 process (the first call on the device does the one-time set-up) and after
@@ -9,6 +20,7 @@ every other test has run.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -17,30 +29,85 @@ from reduction_rdx_sum_gb300 import abi, build, inputs
 
 pytestmark = pytest.mark.gpu
 
+TOL = 1e-6  # |sum - oracle| <= 1e-6 * sum|x_i| + 1e-30 for float32 input
 
-def test_noalloc_sum_matches_rdx_sum_f32_on_two_calls_in_a_row():
+
+def _lib():
     build.build()
     oracle.build()
     lib = abi.load()
-    noalloc = lib.rdx_sum_f32_noalloc
-    noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
-    noalloc.restype = ctypes.c_int
+    fn = lib.rdx_sum_f32_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return lib
+
+
+def _bits(t: torch.Tensor) -> int:
+    return int(t.view(torch.int32).item())
+
+
+def _check_twice(lib, host: np.ndarray, offset: int, stream: torch.cuda.Stream):
+    """rdx_sum_f32 once, then rdx_sum_f32_noalloc twice in a row on `stream`,
+    on the device copy of `host` starting `offset` elements into its buffer."""
+    dev = torch.device("cuda:0")
+    buf = torch.empty(host.size + offset, dtype=torch.float32, device=dev)
+    buf[offset:].copy_(torch.from_numpy(host))
+    x = buf[offset:]
+    ref = torch.full((), float("nan"), dtype=torch.float32, device=dev)
+    gots = [torch.full((), float("nan"), dtype=torch.float32, device=dev) for _ in range(2)]
+    h = stream.cuda_stream
+    torch.cuda.synchronize()
+    assert lib.rdx_sum_f32(x.data_ptr(), x.numel(), ref.data_ptr(), h) == 0, lib.rdx_last_cuda_error()
+    for got in gots:
+        assert lib.rdx_sum_f32_noalloc(x.data_ptr(), x.numel(), got.data_ptr(), h) == 0, lib.rdx_last_cuda_error()
+    stream.synchronize()
+    want = oracle.sum_f32(host)
+    tol = TOL * oracle.abssum_f32(host) + 1e-30
+    for got in gots:
+        assert _bits(got) == _bits(ref), (host.size, offset, got.item(), ref.item())
+        assert abs(got.item() - want) <= tol, (host.size, offset, got.item(), want, tol)
+    del buf
+
+
+@pytest.mark.parametrize("n", [0, 1, 4097, (1 << 24) + 13])
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_noalloc_bitwise_equal_to_rdx_sum_f32_and_within_oracle_tolerance(n, offset):
+    lib = _lib()
+    torch.cuda.set_device(0)
+    host = inputs.normal_f32(n, seed=1) if n > 4097 else inputs.uniform_f32(n, seed=5, lo=-1.0, hi=1.0)
+    side = torch.cuda.Stream(torch.device("cuda:0"))
+    for stream in (side, torch.cuda.default_stream(torch.device("cuda:0"))):
+        _check_twice(lib, host, offset, stream)
+
+
+def test_noalloc_calls_of_different_sizes_back_to_back():
+    """Two calls in a row on different inputs, no host wait between them: the
+    second reuses the scratch (counter and partials) the first one left."""
+    lib = _lib()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev).cuda_stream
-
-    # two inputs of different sizes: the second call reuses the scratch the
-    # first one left behind
     hosts = [inputs.normal_f32((1 << 24) + 13, seed=1), inputs.uniform_f32(1_000_003, seed=5, lo=-1.0, hi=1.0)]
     xs = [torch.from_numpy(h).to(dev) for h in hosts]
     refs = [torch.empty((), dtype=torch.float32, device=dev) for _ in xs]
     gots = [torch.full((), float("nan"), dtype=torch.float32, device=dev) for _ in xs]
+    stream = torch.cuda.current_stream(dev).cuda_stream
     for x, ref in zip(xs, refs):
         assert lib.rdx_sum_f32(x.data_ptr(), x.numel(), ref.data_ptr(), stream) == 0
-    torch.cuda.synchronize()
-    for x, got in zip(xs, gots):           # the two no-allocation calls, back to back
-        assert noalloc(x.data_ptr(), x.numel(), got.data_ptr(), stream) == 0, lib.rdx_last_cuda_error()
+    for x, got in zip(xs, gots):
+        assert lib.rdx_sum_f32_noalloc(x.data_ptr(), x.numel(), got.data_ptr(), stream) == 0, \
+            lib.rdx_last_cuda_error()
     torch.cuda.synchronize()
     for h, ref, got in zip(hosts, refs, gots):
-        tol = 1e-6 * oracle.abssum_f32(h) + 1e-30
-        assert abs(got.item() - ref.item()) <= tol, (got.item(), ref.item(), tol)
+        assert _bits(got) == _bits(ref)
+        assert abs(got.item() - oracle.sum_f32(h)) <= TOL * oracle.abssum_f32(h) + 1e-30
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("offset", [0, 1])
+def test_noalloc_fills_the_static_scratch(offset):
+    """2^28 float32 values (1 GiB): the tiling cuts them into exactly 8192
+    tiles, the most partials the static scratch holds."""
+    lib = _lib()
+    torch.cuda.set_device(0)
+    host = inputs.uniform_f32(1 << 28, seed=3, lo=-1.0, hi=1.0)
+    _check_twice(lib, host, offset, torch.cuda.Stream(torch.device("cuda:0")))

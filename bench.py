@@ -17,6 +17,12 @@ host-to-device copies of the inputs and the device-to-host copies of the
 results are inside its timed region.  ``cpu_baseline`` times the CPU oracle
 (one core) on a bounded sample of the same step.
 
+After the timed region every step's results, and the host copies of the last
+end-to-end step, are compared with the CPU oracle over the whole input
+(bit-exact for the int32 sum, within the float tolerances otherwise, per row
+for row sums), and the steps must agree bit for bit; the line's ``parity``
+object reports it and the exit status is 1 on any mismatch.
+
 ``--impl reference`` times the CPU oracle alone, as the comparison arm, on a
 bounded sample of each step.
 
@@ -361,13 +367,18 @@ class Gb300:
     def event(self):
         return self.torch.cuda.Event(enable_timing=True)
 
-    def step(self, record=None):
-        """One pass of the seven launches, each after an (untimed) L2 flush."""
+    def new_outputs(self):
+        """A fresh output tensor for each of the step's launches."""
+        return [self.torch.full_like(out, -1) for (_, _, _, out) in self.ops]
+
+    def step(self, record=None, outs=None):
+        """One pass of the seven launches, each after an (untimed) L2 flush;
+        results go to `outs` (default: the launches' own output tensors)."""
         for k, (w, fn, x, out) in enumerate(self.ops):
             self.flush()
             if record is not None:
                 record[k][0].record(self.stream)
-            fn(x, out=out, stream=self.stream)
+            fn(x, out=out if outs is None else outs[k], stream=self.stream)
             if record is not None:
                 record[k][1].record(self.stream)
 
@@ -524,7 +535,71 @@ def measure_e2e(g: Gb300, per_config, steps, world):
     secs = max_over_ranks(world, ea.elapsed_time(eb) / 1e3)
     return {"value": round(step_bytes() * steps * world / secs / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "h2d_GBps": round(h2d * steps / secs / 1e9, 1)}
+            "h2d_GBps": round(h2d * steps / secs / 1e9, 1)}, [oh.numpy().copy() for oh in outs_host]
+
+
+# ---------------------------------------------------------------------------
+# parity of the timed results with the oracle
+# ---------------------------------------------------------------------------
+
+TOL_F32, TOL_BF16 = 1e-6, 4e-6   # |gpu - exact| <= tol * sum|term| (+ 1e-30)
+
+
+def oracle_references(arrays):
+    """Oracle value and tolerance of every workload of the step, over the
+    whole input: {name: (reference, tolerance)}; integer sums carry
+    tolerance 0 (bit-exact)."""
+    import oracle
+
+    oracle.build()
+    refs = {}
+    for w in inputs.SUITE:
+        a = arrays[w.name]
+        if w.op == "rowsum_f32":
+            m = a.reshape(w.shape)
+            refs[w.name] = (oracle.rowsum_f32(m), TOL_F32 * oracle.rowabssum_f32(m) + 1e-30)
+        elif w.op == "sum_i32":
+            refs[w.name] = (oracle.sum_i32(a), 0)
+        elif w.op == "sum_f32":
+            refs[w.name] = (oracle.sum_f32(a), TOL_F32 * oracle.abssum_f32(a) + 1e-30)
+        elif w.op == "sumsq_f32":
+            q = oracle.sumsq_f32(a)
+            refs[w.name] = (q, TOL_F32 * q + 1e-30)
+        elif w.op == "sum_bf16":
+            refs[w.name] = (oracle.sum_bf16(a), TOL_BF16 * oracle.abssum_bf16(a) + 1e-30)
+        elif w.op == "sumsq_bf16":
+            q = oracle.sumsq_bf16(a)
+            refs[w.name] = (q, TOL_BF16 * q + 1e-30)
+        else:
+            raise ValueError(w.op)
+    return refs
+
+
+def parity_report(ops, refs, step_results, label):
+    """Compare results with the oracle: per workload the largest
+    |result - oracle| / tolerance over its outputs (0 for an exact integer
+    sum; any value above 1 fails), and whether every step gave the same
+    bits.  step_results: one list of host arrays (one per workload) per
+    step, in the order of `ops`."""
+    report, ok = {}, True
+    for k, (w, _, _, _) in enumerate(ops):
+        first = step_results[0][k]
+        repeat = all(r[k].tobytes() == first.tobytes() for r in step_results[1:])
+        ref, tol = refs[w.name]
+        if w.op == "sum_i32":
+            exact = int(first.reshape(-1)[0]) == int(ref)
+            entry = {"exact": exact, "bitwise_repeat": repeat, "ok": exact and repeat}
+        else:
+            got = first.astype(np.float64).reshape(-1)
+            err = np.abs(got - np.asarray(ref, dtype=np.float64).reshape(-1)) / np.asarray(tol).reshape(-1)
+            worst = float(err.max()) if err.size else 0.0
+            entry = {"max_err_over_tol": round(worst, 6), "bitwise_repeat": repeat,
+                     "ok": bool(np.isfinite(worst) and worst <= 1.0 and repeat)}
+        ok = ok and entry["ok"]
+        report[w.name] = entry
+    report["checked"] = label
+    report["ok"] = ok
+    return report
 
 
 def run_gb300(args):
@@ -542,14 +617,17 @@ def run_gb300(args):
         g.step()
     torch.cuda.synchronize()
 
-    # the timed steps: each launch between two events on its stream
+    # the timed steps: each launch between two events on its stream, each
+    # step into outputs of its own (checked against the oracle afterwards)
     events = [[[g.event(), g.event()] for _ in g.ops] for _ in range(args.steps)]
+    step_outs = [g.new_outputs() for _ in range(args.steps)]
+    torch.cuda.synchronize()
     with ClockSampler(local, os.environ.get("RDX_BENCH_CLOCKS_CSV")) as clk:
         barrier(world)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for s in range(args.steps):
-            g.step(events[s])
+            g.step(events[s], step_outs[s])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         barrier(world)
@@ -574,7 +652,18 @@ def run_gb300(args):
     iters = max(3, min(args.steps, 10))
     extras = measure_extras(g, per_config, iters)
     ladder = measure_ladder(g, iters)
-    e2e = measure_e2e(g, per_config, max(1, min(args.steps, 20)), world)
+    e2e, e2e_results = measure_e2e(g, per_config, max(1, min(args.steps, 20)), world)
+
+    # parity: every timed step's results and the last end-to-end step's host
+    # copies against the oracle over the whole input
+    refs = oracle_references(g.arrays)
+    timed_results = [[o.cpu().numpy() for o in outs] for outs in step_outs]
+    parity = parity_report(g.ops, refs, timed_results,
+                           f"all {args.steps} timed steps against the oracle; bitwise equal across them")
+    parity_e2e = parity_report(g.ops, refs, [e2e_results], "host copies of the last end-to-end step")
+    parity["e2e_ok"] = parity_e2e["ok"]
+    if not parity_e2e["ok"]:
+        parity["e2e"] = parity_e2e
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -589,6 +678,7 @@ def run_gb300(args):
                      "peak_source": f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": e2e,
+        "parity": parity,
         "gpu_launches": len(g.ops) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
@@ -610,13 +700,18 @@ def run_gb300(args):
             "sample": f"first {frac:.2%} of every workload of one step, {passes} pass(es) ({b / 1e6:.0f} MB), "
                       f"one thread, {secs:.1f} s"}
         line["cpu_threads"] = cpu_threads_rate(g.arrays)
+    ok = parity["ok"] and parity["e2e_ok"]
+    if world > 1:
+        ok = max_over_ranks(world, 0.0 if ok else 1.0) == 0.0
     if rank == 0:
         print(json.dumps(line), flush=True)
+        if not ok:
+            print("bench.py: results differ from the oracle (see \"parity\")", file=sys.stderr, flush=True)
     barrier(world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-    return 0
+    return 0 if ok else 1
 
 
 def main(argv=None):

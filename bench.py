@@ -27,7 +27,11 @@ object reports it and the exit status is 1 on any mismatch.
 bounded sample of each step.
 
 Under torchrun each rank reduces its own copy of the workload (weak scaling,
-no collective on the data path); the time is the maximum over ranks.
+no collective on the data path); the time is the maximum over ranks.  The
+line's ``sharded`` object then also times the bf16 and int32 sums split over
+the ranks (strong scaling: a chunk per rank, an NCCL all-gather of the
+partials, the rank-order combine).  On one GPU, ``extras`` times that split
+over 8 chunks emulated on the one device.
 """
 from __future__ import annotations
 
@@ -453,6 +457,17 @@ def measure_extras(g: Gb300, per_config, iters):
         om = torch.empty((), dtype=dt, device=g.dev)
         ms = g.time_launch(lambda: fn(xk, out=om, stream=s), iters)
         extras[name] = figures(ms, xk.numel() * xk.element_size())
+    # the sum split over 8 GPUs, emulated on this one: each chunk's partial
+    # through the one-GPU entry point, then the rank-order combine (9 launches)
+    from reduction_rdx_sum_gb300 import shard
+
+    for name, op, key, dt in (("c5_sum_bf16_split8_emulated", "sum_bf16", key5, torch.float32),
+                              ("c3_sum_i32_split8_emulated", "sum_i32", key3, torch.int64)):
+        xk = g.dev_arrays[key]
+        slots = torch.empty(8, dtype=dt, device=g.dev)
+        res = torch.empty((), dtype=dt, device=g.dev)
+        ms = g.time_launch(lambda: shard.emulate(op, xk, 8, out=res, partials=slots, stream=s), iters)
+        extras[name] = dict(figures(ms, xk.numel() * xk.element_size()), launches=9)
     # narrow rows through shared memory: the same 1 GiB viewed as 3 and 12
     # columns (algorithmic bytes: 4 per element read and 4 per row written)
     flat = g.dev_arrays[g.key(inputs.CFG4_ROWSUM_WIDE)].view(-1)
@@ -482,6 +497,38 @@ def measure_ladder(g: Gb300, iters):
         ladder[f"v{v}"] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
                            "sum_us": round(ms_sum * 1e3, 2), "sum_GB/s": round(nbytes / (ms_sum * 1e-3) / 1e9, 1)}
     return ladder
+
+
+def measure_sharded(g: Gb300, refs, world, rank, iters):
+    """With several ranks: the bf16 sum (2^30 + 7) and the int32 sum (2^28)
+    split over the ranks (strong scaling): each rank reduces its chunk, the
+    partials are all-gathered over NCCL and combined in rank order.  Time per
+    call (L2 flushed before each) is the maximum over ranks; the result must
+    match the oracle on every rank."""
+    from reduction_rdx_sum_gb300 import shard
+
+    torch = g.torch
+    out = {}
+    for w in (inputs.CFG5_SUM_BF16, inputs.CFG3_SUM_I32):
+        x_local = shard.local_chunk(w.op, g.dev_arrays[g.key(w)], world, rank)
+        res = shard.sharded_reduce(w.op, x_local)
+        ts = []
+        for _ in range(iters):
+            g.flush()
+            barrier(world)
+            e0, e1 = g.event(), g.event()
+            e0.record(g.stream)
+            res = shard.sharded_reduce(w.op, x_local)
+            e1.record(g.stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = max_over_ranks(world, float(np.median(ts)))
+        ref, tol = refs[w.name]
+        got = res.item()
+        ok = got == ref if w.op == "sum_i32" else abs(got - ref) <= tol
+        ok = max_over_ranks(world, 0.0 if ok else 1.0) == 0.0
+        out[f"{w.name}_split{world}"] = dict(figures(ms, w.bytes_read), scaling="strong", ranks=world, parity_ok=ok)
+    return out
 
 
 def measure_e2e(g: Gb300, per_config, steps, world):
@@ -664,6 +711,7 @@ def run_gb300(args):
     parity["e2e_ok"] = parity_e2e["ok"]
     if not parity_e2e["ok"]:
         parity["e2e"] = parity_e2e
+    sharded = measure_sharded(g, refs, world, rank, iters) if world > 1 else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -686,6 +734,8 @@ def run_gb300(args):
         "extras": extras,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if sharded is not None:
+        line["sharded"] = sharded
     if rank == 0 and world == 1:
         import oracle
 
@@ -700,7 +750,7 @@ def run_gb300(args):
             "sample": f"first {frac:.2%} of every workload of one step, {passes} pass(es) ({b / 1e6:.0f} MB), "
                       f"one thread, {secs:.1f} s"}
         line["cpu_threads"] = cpu_threads_rate(g.arrays)
-    ok = parity["ok"] and parity["e2e_ok"]
+    ok = parity["ok"] and parity["e2e_ok"] and all(v["parity_ok"] for v in (sharded or {}).values())
     if world > 1:
         ok = max_over_ranks(world, 0.0 if ok else 1.0) == 0.0
     if rank == 0:

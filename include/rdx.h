@@ -278,6 +278,74 @@ rdx_status rdx_ladder_sum_f32(int version, const float* x, int64_t n, float* par
                               cudaStream_t stream);
 
 /*
+ * Reductions split over several GPUs.
+ * Page "03_shared_memory_sync_reduction.py", demo 3: each block leaves one
+ * partial and the partials are added in a second step outside the kernel
+ * (demo 2 of the page: blocks exchange data only by ending the kernel).
+ * Over P GPUs the same two stages appear one level up:
+ *   1. rank r takes the chunk [lo, hi) that rdx_shard_range gives it and
+ *      reduces it with the one-GPU entry point (rdx_sum_f32, ...), leaving
+ *      one partial in device memory;
+ *   2. the caller gathers the P partials into one device array in rank order
+ *      (e.g. an NCCL all-gather; this library runs no collective);
+ *   3. every rank adds them with rdx_combine_* in rank order.
+ * P and the chunking fix every addition, so all ranks get the same bits on
+ * every run.  Row sums split by rows (granule 1) and need no exchange: rank
+ * r's rows are its slice of the output.
+ */
+
+/*
+ * rdx_shard_range: the chunk [*lo, *hi) of rank `rank` among `parts` ranks
+ * sharing n elements.  The elements are cut into whole granules of `granule`
+ * elements; each rank gets floor(G / parts) or one more granule (lower ranks
+ * take the extra ones), the chunks follow one another in rank order, and the
+ * last rank also takes the n mod granule elements after the last whole
+ * granule.  So the chunks tile [0, n), every chunk but the first starts at a
+ * multiple of `granule`, and the split depends on (n, parts, granule) only.
+ * Pass granule = 16 / sizeof(element) (4 for float32 or int32, 8 for
+ * bfloat16) to keep each chunk's 16-byte alignment that of the whole array,
+ * 1 to split rows.  Host only: no CUDA call, no device needed.
+ *   n        elements (or rows), >= 0
+ *   parts    ranks, >= 1;  rank in [0, parts)
+ *   granule  >= 1
+ *   lo, hi   two distinct host int64 slots for the result
+ * Errors: RDX_ERR_INVALID_ARG for any argument outside those ranges.
+ */
+rdx_status rdx_shard_range(int64_t n, int parts, int rank, int64_t granule, int64_t* lo, int64_t* hi);
+
+/* The most partials one rdx_combine_* call adds (4096). */
+int rdx_combine_max_parts(void);
+
+/*
+ * rdx_combine_f32: *out = parts[0] + parts[1] + ... + parts[p-1], float32,
+ * added one by one in index (rank) order: ((parts[0] + parts[1]) + parts[2])
+ * + ...  One small kernel on `stream`; the result is valid in stream order.
+ * Combining the float32 partials of P chunks adds at most P - 1 roundings of
+ * 2^-24 times the running magnitude to the chunks' own error.
+ *   parts  p float32 values in device memory, 4-byte aligned
+ *   p      1 .. rdx_combine_max_parts()
+ *   out    one float32 in device memory, outside parts
+ * Errors: RDX_ERR_INVALID_ARG for a NULL or misaligned pointer, p out of
+ * range, out inside parts; RDX_ERR_CUDA if the launch fails.
+ */
+rdx_status rdx_combine_f32(const float* parts, int p, float* out, cudaStream_t stream);
+
+/*
+ * rdx_combine_f32x2: the same for the [sum, sum of squares] pairs of
+ * rdx_sum_sumsq_*: out2[c] = parts2[0][c] + parts2[1][c] + ... in rank
+ * order, for c = 0, 1.  parts2 holds p pairs (2p float32 values) and out2 one
+ * pair, both 8-byte aligned.  Other arguments and errors as rdx_combine_f32.
+ */
+rdx_status rdx_combine_f32x2(const float* parts2, int p, float* out2, cudaStream_t stream);
+
+/*
+ * rdx_combine_i64: *out = parts[0] + ... + parts[p-1] in int64 (modulo 2^64,
+ * as rdx_sum_i32_i64), exact and independent of the order.  parts and out
+ * are 8-byte aligned.  Other arguments and errors as rdx_combine_f32.
+ */
+rdx_status rdx_combine_i64(const int64_t* parts, int p, int64_t* out, cudaStream_t stream);
+
+/*
  * rdx_sum_f32_noalloc: *out = sum_{i<n} x[i], like rdx_sum_f32, but the call
  * allocates no device memory.  (The paper, the pages this library follows,
  * has no counterpart: this entry point exists for callers of this library,

@@ -87,6 +87,7 @@ def _load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [p, i64], dbl
         lib.oracle_sum_i32.argtypes, lib.oracle_sum_i32.restype = [p, i64], i64
+        lib.oracle_sum_i64.argtypes, lib.oracle_sum_i64.restype = [p, i64], i64
         for name in ("oracle_rowsum_f32", "oracle_rowabssum_f32"):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [p, i64, i64, p], None
@@ -166,6 +167,13 @@ def sum_i32(x: np.ndarray) -> int:
     """Exact int64 sum of int32 values."""
     a = _flat(x, np.int32)
     return int(_load().oracle_sum_i32(_ptr(a), a.size))
+
+
+def sum_i64(x: np.ndarray) -> int:
+    """Sum of int64 values modulo 2^64 (as a signed int64): the combine of
+    the int64 partials of a sum split into chunks."""
+    a = _flat(x, np.int64)
+    return int(_load().oracle_sum_i64(_ptr(a), a.size))
 
 
 # ---- maximum (the page's atomic_max rule, folded from -Inf) ----------------

@@ -138,6 +138,15 @@ int64_t oracle_sum_i32(const int32_t* x, int64_t n) {
     return from_twos_complement(s);
 }
 
+/* The sum of int64 values modulo 2^64: the combine of the int64 partials of
+ * a sum split into chunks (each chunk's int32 sum is one partial; the whole
+ * sum is the sum of the partials, integer addition being associative). */
+int64_t oracle_sum_i64(const int64_t* x, int64_t n) {
+    uint64_t s = 0;
+    for (int64_t i = 0; i < n; ++i) s += (uint64_t)x[i];
+    return from_twos_complement(s);
+}
+
 /* ---- row-segmented float32 sum (row-major, contiguous) ----------------- */
 
 void oracle_rowsum_f32(const float* x, int64_t rows, int64_t cols, double* out) {

@@ -76,6 +76,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
         lib.rdx_ladder_sum_f32.argtypes, lib.rdx_ladder_sum_f32.restype = [i32, vp, i64, vp, vp, vp], i32
+        lib.rdx_shard_range.argtypes = [i64, i32, i32, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.rdx_shard_range.restype = i32
+        lib.rdx_combine_max_parts.argtypes, lib.rdx_combine_max_parts.restype = [], i32
+        for name in ("rdx_combine_f32", "rdx_combine_f32x2", "rdx_combine_i64"):
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = [vp, i32, vp, vp], i32
         lib.rdx_status_string.argtypes, lib.rdx_status_string.restype = [i32], ctypes.c_char_p
         lib.rdx_last_cuda_error.argtypes, lib.rdx_last_cuda_error.restype = [], ctypes.c_char_p
         lib.rdx_shutdown.argtypes, lib.rdx_shutdown.restype = [], None
@@ -305,6 +311,46 @@ def rdx_ladder_sum_f32(version: int, x: torch.Tensor, out: torch.Tensor | None =
                  out.data_ptr())
     _check("rdx_ladder_sum_f32", st)
     return out
+
+
+def rdx_shard_range(n: int, parts: int, rank: int, granule: int) -> tuple[int, int]:
+    """(lo, hi): the chunk of rank ``rank`` among ``parts`` sharing ``n``
+    elements cut in whole granules of ``granule`` elements (host only)."""
+    lo, hi = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("rdx_shard_range", load().rdx_shard_range(n, parts, rank, granule, ctypes.byref(lo), ctypes.byref(hi)))
+    return int(lo.value), int(hi.value)
+
+
+def rdx_combine_max_parts() -> int:
+    return int(load().rdx_combine_max_parts())
+
+
+def _combine(name: str, parts: torch.Tensor, dtype, width: int, out, stream) -> torch.Tensor:
+    lib = load()
+    parts = _input(parts, (dtype,), name)
+    if parts.numel() % width:
+        raise ValueError(f"{name}: expected {width} values per partial")
+    p = parts.numel() // width
+    out = _output(out, parts, dtype, () if width == 1 else (width,))
+    st = _launch(getattr(lib, name), parts.device, stream, parts.data_ptr(), p, out.data_ptr())
+    _check(name, st)
+    return out
+
+
+def rdx_combine_f32(parts: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d float32 tensor: the float32 partials ``parts`` added in index (rank) order."""
+    return _combine("rdx_combine_f32", parts, torch.float32, 1, out, stream)
+
+
+def rdx_combine_f32x2(parts: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """(2,) float32 tensor: the [sum, sum of squares] pairs ``parts`` (p x 2)
+    added component-wise in rank order."""
+    return _combine("rdx_combine_f32x2", parts, torch.float32, 2, out, stream)
+
+
+def rdx_combine_i64(parts: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """0-d int64 tensor: the int64 partials ``parts`` added (modulo 2^64)."""
+    return _combine("rdx_combine_i64", parts, torch.int64, 1, out, stream)
 
 
 def rdx_shutdown() -> None:

@@ -333,6 +333,49 @@ rdx_status rdx_bank_probe(int pattern, int iters, int64_t* cycles, uint32_t* sin
 
 int rdx_bank_probe_loads_per_iter(void) { return rdx::bank_probe_loads_per_iter(); }
 
+rdx_status rdx_shard_range(int64_t n, int parts, int rank, int64_t granule, int64_t* lo, int64_t* hi) {
+    t_last_error.clear();
+    if (lo == nullptr || hi == nullptr || lo == hi) return RDX_ERR_INVALID_ARG;
+    return rdx::shard_range(n, parts, rank, granule, lo, hi) ? RDX_OK : RDX_ERR_INVALID_ARG;
+}
+
+int rdx_combine_max_parts(void) { return rdx::kMaxCombineParts; }
+
+}  // extern "C"
+
+namespace {
+
+rdx_status combine_entry(rdx::CombineType type, size_t bytes, const void* parts, int p, void* out,
+                         cudaStream_t stream) {
+    t_last_error.clear();
+    if (parts == nullptr || out == nullptr || p < 1 || p > rdx::kMaxCombineParts) return RDX_ERR_INVALID_ARG;
+    const size_t align = bytes == 4 ? 4 : 8;
+    if (!is_aligned(parts, align) || !is_aligned(out, align)) return RDX_ERR_INVALID_ARG;
+    if (overlaps(parts, size_t(p) * bytes, out, bytes)) return RDX_ERR_INVALID_ARG;
+    const DeviceCaps* dev = nullptr;
+    const rdx_status st = current_device(&dev);
+    if (st != RDX_OK) return st;
+    const cudaError_t e = rdx::combine_launch(type, parts, p, out, stream);
+    if (e != cudaSuccess) return fail_cuda("combine kernel launch", e);
+    return RDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rdx_status rdx_combine_f32(const float* parts, int p, float* out, cudaStream_t stream) {
+    return combine_entry(rdx::CombineType::F32, 4, parts, p, out, stream);
+}
+
+rdx_status rdx_combine_f32x2(const float* parts2, int p, float* out2, cudaStream_t stream) {
+    return combine_entry(rdx::CombineType::F32x2, 8, parts2, p, out2, stream);
+}
+
+rdx_status rdx_combine_i64(const int64_t* parts, int p, int64_t* out, cudaStream_t stream) {
+    return combine_entry(rdx::CombineType::I64, 8, parts, p, out, stream);
+}
+
 int rdx_debug_build(void) { return RDX_DEBUG ? 1 : 0; }
 
 rdx_status rdx_debug_violations(uint64_t* count, int reset) {
@@ -342,8 +385,8 @@ rdx_status rdx_debug_violations(uint64_t* count, int reset) {
     if (!RDX_DEBUG) return RDX_OK;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda("cudaDeviceSynchronize", e);
-    const unsigned long long parts[3] = {rdx::reduce_out_of_range(reset != 0), rdx::rowsum_out_of_range(reset != 0),
-                                         rdx::ladder_out_of_range(reset != 0)};
+    const unsigned long long parts[4] = {rdx::reduce_out_of_range(reset != 0), rdx::rowsum_out_of_range(reset != 0),
+                                         rdx::ladder_out_of_range(reset != 0), rdx::shard_out_of_range(reset != 0)};
     for (unsigned long long v : parts) {
         if (v == ~0ull) {
             t_last_error = "cudaMemcpyFromSymbol of a violation counter failed";

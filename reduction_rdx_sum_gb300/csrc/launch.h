@@ -102,10 +102,19 @@ int bank_probe_loads_per_iter();
 // One warp; cycles[0] = clock cycles of iters * loads_per_iter loads; sink: 32 words.
 cudaError_t bank_probe_launch(int pattern, int iters, long long* cycles, unsigned* sink, cudaStream_t stream);
 
+// ---- reductions split over several GPUs (shard.cu) ---------------------------
+// Chunk [*lo, *hi) of rank `rank` among `parts` (false for bad arguments).
+bool shard_range(int64_t n, int64_t parts, int64_t rank, int64_t granule, int64_t* lo, int64_t* hi);
+constexpr int kMaxCombineParts = 4096;  // partials one combine adds, at most
+enum class CombineType : int { F32, F32x2, I64 };
+// *out = parts[0] + parts[1] + ... + parts[p - 1], added in that order.
+cudaError_t combine_launch(CombineType type, const void* parts, int p, void* out, cudaStream_t stream);
+
 // ---- checked build (RDX_DEBUG=1): out-of-range accesses caught, per file ------
 unsigned long long reduce_out_of_range(bool reset);
 unsigned long long rowsum_out_of_range(bool reset);
 unsigned long long ladder_out_of_range(bool reset);
+unsigned long long shard_out_of_range(bool reset);
 
 // ---- error text shared by every entry point (api.cu) ------------------------
 // Replace the calling thread's rdx_last_cuda_error() text.

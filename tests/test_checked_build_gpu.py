@@ -158,3 +158,22 @@ def test_ladder_sum_stays_in_bounds(lib):
             assert np.array_equal(parts.cpu().numpy(), oracle.ladder_partials(v, host))
             check("sum_f32", host, out.item())
     assert violations(lib) == 0
+
+
+def test_combine_stays_in_bounds(lib):
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    for name in ("rdx_combine_f32", "rdx_combine_f32x2", "rdx_combine_i64"):
+        getattr(lib, name).argtypes = [vp, i32, vp, vp]
+    for p in (1, 2, 257, 4096):
+        parts = inputs.normal_f32(2 * p, seed=p)
+        x = torch.from_numpy(parts).to(DEV)
+        out = torch.empty(2, device=DEV)
+        assert lib.rdx_combine_f32(x.data_ptr(), p, out.data_ptr(), stream()) == 0
+        assert lib.rdx_combine_f32x2(x.data_ptr(), p, out.data_ptr(), stream()) == 0
+        ints = torch.from_numpy(np.arange(p, dtype=np.int64) - 7).to(DEV)
+        tot = torch.empty((), dtype=torch.int64, device=DEV)
+        assert lib.rdx_combine_i64(ints.data_ptr(), p, tot.data_ptr(), stream()) == 0
+        torch.cuda.synchronize()
+        assert tot.item() == p * (p - 1) // 2 - 7 * p
+        assert abs(out[0].item() - oracle.sum_f32(parts[0::2])) <= p * 2.0 ** -24 * oracle.abssum_f32(parts) + 1e-30
+    assert violations(lib) == 0

@@ -31,6 +31,10 @@ C_MUTANTS = [
     ("bf16 widened by 15 bits", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
     ("int sum in 32 bits", "for (int64_t i = 0; i < n; ++i) s += (uint64_t)(int64_t)x[i];",
      "for (int64_t i = 0; i < n; ++i) s = (uint32_t)(s + (uint64_t)(int64_t)x[i]);"),
+    ("int64 sum drops the last", "    for (int64_t i = 0; i < n; ++i) s += (uint64_t)x[i];",
+     "    for (int64_t i = 0; i + 1 < n; ++i) s += (uint64_t)x[i];"),
+    ("int64 sum saturates instead of wrapping", "    for (int64_t i = 0; i < n; ++i) s += (uint64_t)x[i];\n    return from_twos_complement(s);",
+     "    long double t = 0;\n    for (int64_t i = 0; i < n; ++i) t += (long double)x[i];\n    (void)s;\n    return t > 9.2e18L ? INT64_MAX : t < -9.2e18L ? INT64_MIN : (int64_t)t;"),
     ("row stride off by one", "const float* row = x + r * cols;\n        kahan_acc k;\n        kahan_init(&k);\n        for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);",
      "const float* row = x + r * (cols + (r > 0));\n        kahan_acc k;\n        kahan_init(&k);\n        for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);"),
     ("rows summed as columns", "for (int64_t j = 0; j < cols; ++j) kahan_add(&k, (double)row[j]);\n        out[r] = kahan_result(&k);",
@@ -58,6 +62,8 @@ def pin_battery():
         ("brute force f32", lambda: [op.test_brute_force_f32(n, d) for n in (7, 33, 64)
                                      for d in ("uniform", "normal", "wide", "cancel")]),
         ("brute force i32", lambda: [op.test_brute_force_i32(n) for n in (5, 64)]),
+        ("i64 closed forms", lambda: [op.test_sum_i64_closed_forms(n) for n in (1, 33)]),
+        ("brute force i64", lambda: [op.test_brute_force_i64(n) for n in (5, 64)]),
         ("brute force bf16", lambda: [op.test_brute_force_bf16(n) for n in (7, 64)]),
         ("compensation", op.test_kahan_compensation_is_present),
         ("non-finite", op.test_nonfinite_propagation),

@@ -67,10 +67,39 @@ def test_sum_i32_closed_forms(n):
     assert oracle.sum_i32(x) == n * (n - 1) // 2
 
 
+def _wrap64(v: int) -> int:
+    """v modulo 2^64, as a signed int64."""
+    v &= (1 << 64) - 1
+    return v - (1 << 64) if v >= 1 << 63 else v
+
+
+@pytest.mark.parametrize("n", [1, 2, 33, 4096])
+def test_sum_i64_closed_forms(n):
+    assert oracle.sum_i64(np.full(n, -3, np.int64)) == -3 * n
+    x = np.arange(n, dtype=np.int64) * (1 << 32)
+    assert oracle.sum_i64(x) == (n * (n - 1) // 2) * (1 << 32)
+    # addition modulo 2^64: 2^62 four times wraps to 0; INT64_MAX + 1 to INT64_MIN
+    assert oracle.sum_i64(np.full(4 * n, 1 << 62, np.int64)) == 0
+    assert oracle.sum_i64(np.array([2 ** 63 - 1] + [1] * n, np.int64)) == -(2 ** 63) + n - 1
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 1000])
+def test_brute_force_i64(n):
+    rng = np.random.default_rng(100 + n)
+    x = rng.integers(-(2 ** 63), 2 ** 63 - 1, n, dtype=np.int64, endpoint=True)
+    assert oracle.sum_i64(x) == _wrap64(sum(int(v) for v in x))
+    # the combine of chunk sums is the whole sum: split int32 data anywhere
+    z = rng.integers(-(2 ** 31), 2 ** 31, 3 * n + 1, dtype=np.int64).astype(np.int32)
+    cuts = sorted(rng.integers(0, z.size + 1, 4))
+    parts = [oracle.sum_i32(c) for c in np.split(z, cuts)]
+    assert oracle.sum_i64(np.array(parts, np.int64)) == oracle.sum_i32(z)
+
+
 def test_sum_empty():
     assert oracle.sum_f32(np.zeros(0, np.float32)) == 0.0
     assert oracle.sum_bf16(np.zeros(0, np.uint16)) == 0.0
     assert oracle.sum_i32(np.zeros(0, np.int32)) == 0
+    assert oracle.sum_i64(np.zeros(0, np.int64)) == 0
     assert oracle.rowsum_f32(np.zeros((0, 5), np.float32)).shape == (0,)
     assert np.all(oracle.rowsum_f32(np.zeros((4, 0), np.float32)) == 0.0)
 

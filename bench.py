@@ -481,21 +481,28 @@ def measure_extras(g: Gb300, per_config, iters):
     return extras
 
 
-def measure_ladder(g: Gb300, iters):
-    """The page's five block reductions on the config-2 float32 array: the
-    partials alone (the page's kernel), and the whole sum with the device
-    finish in the same launch (comparable with c2_sum_f32)."""
-    x2 = g.dev_arrays[g.key(inputs.CFG2_SUM_F32)]
-    nbytes = x2.numel() * 4
-    total = g.torch.empty((), dtype=g.torch.float32, device=g.dev)
-    ladder = {}
+def measure_ladder(g: Gb300, launches=5):
+    """The page's five block reductions on a float32 input larger than the
+    L2 (config 4's 1 GiB of U[-1,1) values, n = 2^28): the partials alone
+    (the page's kernel) and the whole sum with the device finish in the same
+    launch, each as `launches` back-to-back launches between two events (the
+    input streams from HBM every time; many launches put the timer's 2 us
+    tick far below the differences between versions).  rdx_sum_f32 on the
+    same input, timed the same way, for comparison."""
+    torch, abi = g.torch, g.abi
+    x = g.dev_arrays[g.key(inputs.CFG4_ROWSUM_WIDE)].view(torch.float32)
+    nbytes = x.numel() * 4
+    total = torch.empty((), dtype=torch.float32, device=g.dev)
+    ladder = {"n": x.numel(), "launches": launches}
     for v in range(1, 6):
-        part = g.torch.empty(g.abi.rdx_ladder_num_partials(v, x2.numel()), dtype=g.torch.float32, device=g.dev)
-        ms = g.time_launch(lambda: g.abi.rdx_ladder_partials_f32(v, x2, out=part, stream=g.stream), iters)
-        ms_sum = g.time_launch(lambda: g.abi.rdx_ladder_sum_f32(v, x2, out=total, partials=part, stream=g.stream),
-                               iters)
-        ladder[f"v{v}"] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                           "sum_us": round(ms_sum * 1e3, 2), "sum_GB/s": round(nbytes / (ms_sum * 1e-3) / 1e9, 1)}
+        part = torch.empty(abi.rdx_ladder_num_partials(v, x.numel()), dtype=torch.float32, device=g.dev)
+        ms = g.time_back_to_back(lambda: abi.rdx_ladder_partials_f32(v, x, out=part, stream=g.stream), launches)
+        ms_sum = g.time_back_to_back(lambda: abi.rdx_ladder_sum_f32(v, x, out=total, partials=part, stream=g.stream),
+                                     launches)
+        ladder[f"v{v}"] = {"us": round(ms * 1e3, 1), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                           "sum_us": round(ms_sum * 1e3, 1), "sum_GB/s": round(nbytes / (ms_sum * 1e-3) / 1e9, 1)}
+    ms = g.time_back_to_back(lambda: abi.rdx_sum_f32(x, out=total, stream=g.stream), launches)
+    ladder["rdx_sum_f32"] = {"us": round(ms * 1e3, 1), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     return ladder
 
 
@@ -698,7 +705,7 @@ def run_gb300(args):
 
     iters = max(3, min(args.steps, 10))
     extras = measure_extras(g, per_config, iters)
-    ladder = measure_ladder(g, iters)
+    ladder = measure_ladder(g)
     e2e, e2e_results = measure_e2e(g, per_config, max(1, min(args.steps, 20)), world)
 
     # parity: every timed step's results and the last end-to-end step's host
@@ -730,7 +737,7 @@ def run_gb300(args):
         "gpu_launches": len(g.ops) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
-        "ladder_fp32_n2^24+13": ladder,
+        "ladder_fp32_n2^28": ladder,
         "extras": extras,
         "kernel_source_hash": kernel_source_hash(),
     }

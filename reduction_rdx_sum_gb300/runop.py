@@ -6,6 +6,7 @@ For quick timings and for profilers (one kernel, a few launches, a chosen size):
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 262144 --cols 256
     python -m reduction_rdx_sum_gb300.runop --config c5_sum_bf16     # a workload of the suite
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 16777216 --cols 16 --offset 1
+    python -m reduction_rdx_sum_gb300.runop --op ladder_partials --version 2 --n 262144 --input page
 
 Before each timed call the L2 is flushed (a write of 512 MiB, then a read of
 512 MiB so that no dirty line is left for the timed kernel to write back).
@@ -23,7 +24,7 @@ import torch
 from . import abi, inputs
 
 OPS = ("sum_f32", "sumsq_f32", "sum_bf16", "sumsq_bf16", "sum_i32", "rowsum_f32", "sum_f32_noalloc",
-       "sum_sumsq_f32", "sum_sumsq_bf16", "max_f32", "max_i32", "bank_probe")
+       "sum_sumsq_f32", "sum_sumsq_bf16", "max_f32", "max_i32", "bank_probe", "ladder_partials", "ladder_sum")
 
 
 def make_input(op: str, n: int, rows: int, cols: int, seed: int, dev) -> torch.Tensor:
@@ -36,7 +37,11 @@ def make_input(op: str, n: int, rows: int, cols: int, seed: int, dev) -> torch.T
     return torch.from_numpy(inputs.normal_f32(n, seed)).to(dev)
 
 
-def entry(op: str):
+def entry(op: str, version: int = 5):
+    if op == "ladder_partials":
+        return lambda x, stream=None: abi.rdx_ladder_partials_f32(version, x, stream=stream)
+    if op == "ladder_sum":
+        return lambda x, stream=None: abi.rdx_ladder_sum_f32(version, x, stream=stream)
     if op == "rowsum_f32":
         return abi.rdx_rowsum_f32
     if op == "sum_f32_noalloc":
@@ -73,6 +78,10 @@ def main(argv=None) -> int:
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--offset", type=int, default=0,
                     help="start the input this many elements into its allocation (a base off 16-byte alignment)")
+    ap.add_argument("--version", type=int, default=5, choices=range(1, 6),
+                    help="the page's block-reduction version for ladder_partials / ladder_sum")
+    ap.add_argument("--input", choices=("seeded", "page"), default="seeded",
+                    help="page: the page's own float32 input arange(n) %% 7 (float ops only)")
     args = ap.parse_args(argv)
     if args.offset < 0:
         ap.error("--offset must be >= 0")
@@ -93,12 +102,14 @@ def main(argv=None) -> int:
         host = host.view(np.int16) if host.dtype == np.uint16 else host
         x = torch.from_numpy(host.reshape(w.shape)).to(dev)
         args.op = w.op
+    elif args.input == "page":
+        x = torch.from_numpy((np.arange(args.n) % 7).astype(np.float32)).to(dev)
     else:
         x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
     if args.offset:
         buf = torch.empty(x.numel() + args.offset, dtype=x.dtype, device=dev)
         x = buf[args.offset:].view(x.shape).copy_(x)
-    fn = entry(args.op)
+    fn = entry(args.op, args.version)
     stream = torch.cuda.current_stream(dev)
     flush = None if args.no_flush else L2Flush(dev)
     nbytes = x.numel() * x.element_size()

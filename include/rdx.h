@@ -220,6 +220,22 @@ rdx_status rdx_rowsum_strided_f32(const float* x, int64_t rows, int64_t cols, in
 size_t rdx_workspace_bytes(void);
 
 /*
+ * Kernels one call enqueues on its stream (for callers that count launches
+ * or capture graphs).  A scalar reduction (and the row sum of few, very long
+ * rows) cuts its input into tiles, one block each; with tiles of 64 KiB or
+ * more (inputs of 64 MiB and up) the fixed-order pass over the tile partials
+ * runs as a second kernel, launched behind the first with programmatic
+ * dependent launch, instead of in the first kernel's last block (so no block
+ * waits on a completion ticket; both give the same bits).
+ * rdx_reduce_kernels: 1 or 2 for rdx_reduce_ws code `op` (or its named entry
+ * point) on n elements; -1 for a bad op or n < 0.
+ * rdx_rowsum_kernels: 0 (rows == 0), 1 or 2 for rdx_rowsum_f32 on a
+ * rows x cols matrix; -1 for negative sizes.
+ */
+int rdx_reduce_kernels(int op, int64_t n);
+int rdx_rowsum_kernels(int64_t rows, int64_t cols);
+
+/*
  * rdx_reduce_ws: the scalar reduction `op` (an RDX_OP_* code) of n elements
  * of x into out, with a workspace the caller owns instead of the library's.
  * Results are the same as the named entry point's (same kernel and tiling).

@@ -66,6 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.rdx_rowsum_strided_f32.argtypes = [vp, i64, i64, i64, vp, vp]
         lib.rdx_rowsum_strided_f32.restype = i32
         lib.rdx_workspace_bytes.argtypes, lib.rdx_workspace_bytes.restype = [], ctypes.c_size_t
+        lib.rdx_reduce_kernels.argtypes, lib.rdx_reduce_kernels.restype = [i32, i64], i32
+        lib.rdx_rowsum_kernels.argtypes, lib.rdx_rowsum_kernels.restype = [i64, i64], i32
         lib.rdx_reduce_ws.argtypes = [i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
         lib.rdx_reduce_ws.restype = i32
         lib.rdx_bank_probe.argtypes, lib.rdx_bank_probe.restype = [i32, i32, vp, vp, vp], i32
@@ -233,6 +235,16 @@ _OP_OUT = {0: (torch.float32, ()), 1: (torch.float32, ()), 2: (torch.float32, ()
 
 def rdx_workspace_bytes() -> int:
     return int(load().rdx_workspace_bytes())
+
+
+def rdx_reduce_kernels(op, n: int) -> int:
+    """Kernels one call of scalar reduction ``op`` (name or RDX_OP_* code) on n elements enqueues."""
+    return int(load().rdx_reduce_kernels(OP_CODES[op] if isinstance(op, str) else int(op), n))
+
+
+def rdx_rowsum_kernels(rows: int, cols: int) -> int:
+    """Kernels one rdx_rowsum_f32 call on a rows x cols matrix enqueues."""
+    return int(load().rdx_rowsum_kernels(rows, cols))
 
 
 def rdx_reduce_ws(op, x: torch.Tensor, workspace: torch.Tensor, out: torch.Tensor | None = None,

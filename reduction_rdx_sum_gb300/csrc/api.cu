@@ -239,6 +239,18 @@ rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t s
 
 size_t rdx_workspace_bytes(void) { return workspace_bytes(); }
 
+int rdx_reduce_kernels(int op, int64_t n) {
+    if (!valid_op(op) || n < 0) return -1;
+    return rdx::reduce_plan(Op(op), 1, n).separate_finish ? 2 : 1;
+}
+
+int rdx_rowsum_kernels(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0) return -1;
+    if (rows == 0) return 0;
+    if (!rdx::rowsum_use_split(rows, cols)) return 1;
+    return rdx::reduce_plan(Op::SumF32, rows, cols).separate_finish ? 2 : 1;
+}
+
 rdx_status rdx_reduce_ws(int op, const void* x, int64_t n, void* out, void* workspace, size_t workspace_size,
                          cudaStream_t stream) {
     t_last_error.clear();

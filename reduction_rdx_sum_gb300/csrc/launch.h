@@ -65,6 +65,9 @@ struct ReducePlan {
     int64_t tile = 0;
     int64_t tiles = 1;
     bool large = false;  // the deeper kernel variant (8 loads in flight, 4 blocks per SM)
+    // the finish runs as a second kernel (one block per row) after the tiles'
+    // grid instead of in its last block; only when tiles > 1
+    bool separate_finish = false;
 };
 int reduce_block_threads();
 int64_t reduce_max_partials();
@@ -78,9 +81,10 @@ ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols);
 bool reduce_uses_words(Op op);
 // partials: rows * plan.tiles slots (reduce_acc_bytes each; not touched by
 // the word-finishing ops); counters: rows zeroed completion counters, left
-// zeroed; words: one zeroed 8-byte accumulator word, left zeroed (only the
-// word-finishing ops touch it; it may be NULL for the others).  None of these
-// is touched when plan.tiles == 1.  out: rows results.
+// zeroed (not touched when plan.separate_finish); words: one zeroed 8-byte
+// accumulator word, left zeroed (only the word-finishing ops touch it; it may
+// be NULL for the others).  None of these is touched when plan.tiles == 1.
+// out: rows results.  Enqueues one kernel, or two when plan.separate_finish.
 cudaError_t reduce_launch(Op op, const void* x, int64_t rows, int64_t cols, int64_t ld, const ReducePlan& plan,
                           void* partials, unsigned* counters, unsigned long long* words, void* out,
                           cudaStream_t stream);

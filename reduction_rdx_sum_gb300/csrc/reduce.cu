@@ -43,6 +43,9 @@
 #ifndef RDX_REDUCE_MIN_TILE
 #define RDX_REDUCE_MIN_TILE 1024
 #endif
+#ifndef RDX_SEPARATE_FINISH_MIN_TILE
+#define RDX_SEPARATE_FINISH_MIN_TILE 4096
+#endif
 
 namespace rdx {
 namespace {
@@ -55,6 +58,12 @@ constexpr int64_t kMinTile = RDX_REDUCE_MIN_TILE;         // 16-byte vectors per
 constexpr int64_t kMidTiles = 1024;                       // tiles aimed at for mid-size inputs
 constexpr int64_t kMidTileCap = 4096;                     // largest tile of the mid-size rule (64 KiB)
 constexpr int kFinishLoadBytes = 32;                      // partial bytes in flight per thread, last block
+// Tiles of at least this many 16-byte vectors (64 KiB: inputs of 64 MiB and
+// up) finish in a second kernel instead of the last block.  Measured, fp32,
+// L2 flushed, means of 61: 64 MiB 17.6 -> 17.0 us, 256 MiB 44.6 -> 43.4 us,
+// 1 GiB 149.1 -> 148.7 us; with shorter tiles the second launch costs more
+// than the tickets it saves (16 MiB 9.9 -> 10.7 us).
+constexpr int64_t kSeparateFinishMinTile = RDX_SEPARATE_FINISH_MIN_TILE;
 // 8 resident blocks of 256 threads fill an SM (2048 threads): at most 32
 // registers per thread, so every dtype streams with full occupancy.
 constexpr int kMinBlocksPerSm = 2048 / kBlock;
@@ -68,7 +77,41 @@ static_assert((kUnroll & (kUnroll - 1)) == 0 && (kUnrollLarge & (kUnrollLarge - 
               "load batches are powers of two");
 static_assert(kMinTile % kBlock == 0, "tiles are whole multiples of the block");
 
-template <class P, int U, int kMinBlocks>
+// The fixed-order pass over one row's g partials rp[0 .. g): thread t adds
+// partials t, t + kBlock, ... (kFinishUnroll independent chains, their loads
+// in flight together), then the block tree.  The result is valid in thread 0.
+// Loads go through L2 (other blocks, or another grid, wrote the partials).
+template <class P>
+__device__ __forceinline__ typename P::Acc finish_row(const typename P::Acc* __restrict__ rp, int g,
+                                                      const void* part_lo, size_t part_span,
+                                                      typename P::Acc* smem) {
+    using Acc = typename P::Acc;
+    constexpr int kFinishUnroll = kFinishLoadBytes / int(sizeof(Acc));
+    Acc b[kFinishUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinishUnroll; ++u) b[u] = P::identity();
+    int j = threadIdx.x;
+    for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
+        Acc p[kFinishUnroll];
+#pragma unroll
+        for (int u = 0; u < kFinishUnroll; ++u)
+            p[u] = guard(rp + j + u * kBlock, sizeof(Acc), part_lo, part_span) ? load_cg(rp + j + u * kBlock)
+                                                                             : P::identity();
+#pragma unroll
+        for (int u = 0; u < kFinishUnroll; ++u) b[u] += p[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kFinishUnroll; ++u) {
+        if (j + u * kBlock < g && guard(rp + j + u * kBlock, sizeof(Acc), part_lo, part_span))
+            b[u] += load_cg(rp + j + u * kBlock);
+    }
+    return block_sum<kBlock>(fold_array(b), smem, P::identity());
+}
+
+// kSeparate: the grid leaves the finish to finish_kernel, launched right
+// after it on the same stream: every block only stores its partial (or folds
+// its total into the accumulator word) and exits, with no ticket to wait for.
+template <class P, int U, int kMinBlocks, bool kSeparate>
 __global__ void __launch_bounds__(kBlock, kMinBlocks)
 reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, int64_t tile,
               typename P::Acc* __restrict__ partials, unsigned* __restrict__ counters,
@@ -144,6 +187,7 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
             unsigned long long* word = words + row;
             const size_t word_span = size_t(gridDim.y) * sizeof(unsigned long long);
             if (guard(word, sizeof *word, words, word_span)) P::fold_word(word, a);
+            if (kSeparate) return;
             if (guard(counter, sizeof(unsigned), counters, gridDim.y * sizeof(unsigned)) &&
                 take_ticket(counter) == gridDim.x - 1) {
                 const Acc total = guard(word, sizeof *word, words, word_span) ? P::take_word(word) : P::identity();
@@ -155,6 +199,10 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     }
     Acc* __restrict__ rp = partials + row * int64_t(gridDim.x);
     const size_t part_span = size_t(gridDim.x) * gridDim.y * sizeof(Acc);
+    if (kSeparate) {
+        if (threadIdx.x == 0 && guard(rp + blockIdx.x, sizeof(Acc), partials, part_span)) rp[blockIdx.x] = a;
+        return;
+    }
     if (threadIdx.x == 0) {
         if (guard(rp + blockIdx.x, sizeof(Acc), partials, part_span)) rp[blockIdx.x] = a;
         last_block = guard(counter, sizeof(unsigned), counters, gridDim.y * sizeof(unsigned))
@@ -164,34 +212,41 @@ reduce_kernel(const typename P::In* __restrict__ x, int64_t cols, int64_t ld, in
     __syncthreads();
     if (!last_block) return;
 
-    // The row's last block: every partial of the row is in place.  Thread t
-    // adds partials t, t + kBlock, ... (kFinishUnroll independent chains,
-    // loads in flight together), then the block tree.
-    constexpr int kFinishUnroll = kFinishLoadBytes / int(sizeof(Acc));
-    Acc b[kFinishUnroll];
-#pragma unroll
-    for (int u = 0; u < kFinishUnroll; ++u) b[u] = P::identity();
-    const int g = int(gridDim.x);
-    int j = threadIdx.x;
-    for (; j + (kFinishUnroll - 1) * kBlock < g; j += kFinishUnroll * kBlock) {
-        Acc p[kFinishUnroll];
-#pragma unroll
-        for (int u = 0; u < kFinishUnroll; ++u)
-            p[u] = guard(rp + j + u * kBlock, sizeof(Acc), partials, part_span) ? load_cg(rp + j + u * kBlock)
-                                                                              : P::identity();
-#pragma unroll
-        for (int u = 0; u < kFinishUnroll; ++u) b[u] += p[u];
-    }
-#pragma unroll
-    for (int u = 0; u < kFinishUnroll; ++u) {
-        if (j + u * kBlock < g && guard(rp + j + u * kBlock, sizeof(Acc), partials, part_span))
-            b[u] += load_cg(rp + j + u * kBlock);
-    }
-    const Acc total = block_sum<kBlock>(fold_array(b), smem, P::identity());
+    // The row's last block: every partial of the row is in place.
+    const Acc total = finish_row<P>(rp, int(gridDim.x), partials, part_span, smem);
     if (threadIdx.x == 0) {
         if (guard(out + row, sizeof(Acc), out, out_span)) out[row] = total;
         *counter = 0u;  // ready for the next call on this stream (checked above)
     }
+}
+
+// The finish of a kSeparate grid: one block per row, launched behind it with
+// programmatic dependent launch.  griddepcontrol.wait returns once that grid
+// has completed and its writes are visible, so every partial (or the whole
+// accumulator word) is in place.  The same fixed-order pass as the last
+// block's above, so the result has the same bits either way.
+template <class P>
+__global__ void __launch_bounds__(kBlock)
+finish_kernel(const typename P::Acc* __restrict__ partials, int64_t tiles, unsigned long long* __restrict__ words,
+              typename P::Acc* __restrict__ out) {
+    using Acc = typename P::Acc;
+    __shared__ Acc smem[kBlock / kWarpSize];
+    pdl_wait();
+    pdl_release();
+    const int64_t row = blockIdx.x;
+    const size_t out_span = size_t(gridDim.x) * sizeof(Acc);
+    if constexpr (has_word_finish<P>::value) {
+        if (threadIdx.x == 0) {
+            unsigned long long* word = words + row;
+            const size_t word_span = size_t(gridDim.x) * sizeof(unsigned long long);
+            const Acc total = guard(word, sizeof *word, words, word_span) ? P::take_word(word) : P::identity();
+            if (guard(out + row, sizeof(Acc), out, out_span)) out[row] = total;
+        }
+        return;
+    }
+    const size_t part_span = size_t(tiles) * gridDim.x * sizeof(Acc);
+    const Acc total = finish_row<P>(partials + row * tiles, int(tiles), partials, part_span, smem);
+    if (threadIdx.x == 0 && guard(out + row, sizeof(Acc), out, out_span)) out[row] = total;
 }
 
 template <class P>
@@ -202,11 +257,21 @@ cudaError_t launch_typed(const void* x, int64_t rows, int64_t cols, int64_t ld, 
     const auto* xt = static_cast<const typename P::In*>(x);
     auto* pt = static_cast<typename P::Acc*>(partials);
     auto* ot = static_cast<typename P::Acc*>(out);
+    cudaError_t e;
+    if (plan.separate_finish) {
+        e = plan.large ? launch_pdl(reduce_kernel<P, kUnrollLarge, kMinBlocksLarge, true>, grid, dim3(kBlock), stream,
+                                    xt, cols, ld, plan.tile, pt, counters, words, ot)
+                       : launch_pdl(reduce_kernel<P, kUnroll, kMinBlocksPerSm, true>, grid, dim3(kBlock), stream, xt,
+                                    cols, ld, plan.tile, pt, counters, words, ot);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(finish_kernel<P>, dim3(unsigned(rows)), dim3(kBlock), stream,
+                          static_cast<const typename P::Acc*>(pt), plan.tiles, words, ot);
+    }
     if (plan.large)
-        return launch_pdl(reduce_kernel<P, kUnrollLarge, kMinBlocksLarge>, grid, dim3(kBlock), stream, xt, cols, ld,
-                          plan.tile, pt, counters, words, ot);
-    return launch_pdl(reduce_kernel<P, kUnroll, kMinBlocksPerSm>, grid, dim3(kBlock), stream, xt, cols, ld, plan.tile,
-                      pt, counters, words, ot);
+        return launch_pdl(reduce_kernel<P, kUnrollLarge, kMinBlocksLarge, false>, grid, dim3(kBlock), stream, xt, cols,
+                          ld, plan.tile, pt, counters, words, ot);
+    return launch_pdl(reduce_kernel<P, kUnroll, kMinBlocksPerSm, false>, grid, dim3(kBlock), stream, xt, cols, ld,
+                      plan.tile, pt, counters, words, ot);
 }
 
 }  // namespace
@@ -251,6 +316,8 @@ ReducePlan reduce_plan(Op op, int64_t rows, int64_t cols) {
     p.tiles = mmax > 0 ? (mmax + tile - 1) / tile : 1;
     // many waves of tiles long enough for whole batches of the deeper kernel
     p.large = r * p.tiles >= kLargeTiles && tile >= kUnrollLarge * kBlock;
+    // long tiles: the finish in a kernel of its own (blocks exit without a ticket)
+    p.separate_finish = p.tiles > 1 && tile >= kSeparateFinishMinTile;
     return p;
 }
 

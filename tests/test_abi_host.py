@@ -162,3 +162,19 @@ def test_normal_build_is_unchecked(lib):
     count = ctypes.c_uint64(7)
     assert f(ctypes.byref(count), 0) == abi.RDX_OK and count.value == 0   # no CUDA call in a normal build
     assert f(None, 0) == INVALID
+
+
+def test_kernel_counts_per_call(lib):
+    # tiles of 64 KiB and more finish in a second kernel; shorter ones in the last block
+    assert abi.rdx_reduce_kernels("sum_f32", 0) == 1
+    assert abi.rdx_reduce_kernels("sum_f32", 1 << 20) == 1
+    assert abi.rdx_reduce_kernels("sum_f32", (1 << 22) + 13) == 1
+    assert abi.rdx_reduce_kernels("sum_f32", (1 << 24) + 13) == 2
+    assert abi.rdx_reduce_kernels("sum_i32", 1 << 28) == 2
+    assert abi.rdx_reduce_kernels("sum_bf16", (1 << 30) + 7) == 2
+    assert abi.rdx_reduce_kernels("max_i32", 1 << 28) == 2
+    assert abi.rdx_reduce_kernels(99, 10) == -1 and abi.rdx_reduce_kernels("sum_f32", -1) == -1
+    assert abi.rdx_rowsum_kernels(0, 5) == 0
+    assert abi.rdx_rowsum_kernels(8192, 32768) == 1 and abi.rdx_rowsum_kernels(1 << 20, 256) == 1
+    assert abi.rdx_rowsum_kernels(4, 1 << 26) == 2
+    assert abi.rdx_rowsum_kernels(-1, 5) == -1

@@ -64,17 +64,17 @@ FLUSH_BYTES = 512 << 20
 # by the element count (traffic grows in proportion).
 _RED = ("device.cuh", "reduce.cu")
 _ROW = ("device.cuh", "rowsum.cu")
-_RED_HASH = "a6f536c6cc94ecd4"
+_RED_HASH = "64a04e1696a0e1b1"
 _ROW_HASH = "fda490a938249909"
 NCU_TRAFFIC = {
     # workload: bytes per full launch, scaled from the capture named in the profile
-    "c5_sum_bf16": {"bytes_per_launch": 2160056334, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sum_bf16": {"bytes_per_launch": 2160423950, "sources": _RED, "source_hash": _RED_HASH,
                     "profile": "profiles/reduce_kernel_SumBF16_bf16_n268435456.md"},
-    "c5_sumsq_bf16": {"bytes_per_launch": 2159155214, "sources": _RED, "source_hash": _RED_HASH,
+    "c5_sumsq_bf16": {"bytes_per_launch": 2158738446, "sources": _RED, "source_hash": _RED_HASH,
                       "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c3_sum_i32": {"bytes_per_launch": 1079200768, "sources": _RED, "source_hash": _RED_HASH,
+    "c3_sum_i32": {"bytes_per_launch": 1078776832, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
-    "c2_sum_f32": {"bytes_per_launch": 67259648, "sources": _RED, "source_hash": _RED_HASH,
+    "c2_sum_f32": {"bytes_per_launch": 67197440, "sources": _RED, "source_hash": _RED_HASH,
                    "profile": "profiles/kernels_dram_traffic_small_cases.md"},
     "c4_rowsum_8192x32768": {"bytes_per_launch": 1080155136, "sources": _ROW, "source_hash": _ROW_HASH,
                              "profile": "profiles/kernels_dram_traffic_small_cases.md"},
@@ -572,25 +572,53 @@ def measure_e2e(g: Gb300, per_config, steps, world):
     order = sorted(g.distinct, key=lambda k: -compute_us[k])
     copy_stream = torch.cuda.Stream(g.dev)
 
-    def e2e_step():
+    def e2e_step(timeline=None):
         copy_stream.wait_stream(s)
+        if timeline is not None:
+            timeline["start"] = g.event()
+            timeline["start"].record(copy_stream)
         landed = {}
         with torch.cuda.stream(copy_stream):
             for key in order:
                 g.dev_arrays[key].copy_(pinned[key], non_blocking=True)
-                landed[key] = torch.cuda.Event()
+                landed[key] = g.event() if timeline is not None else torch.cuda.Event()
                 landed[key].record(copy_stream)
         for key in order:
             s.wait_event(landed[key])
             for (w, fn, x, out) in g.ops:
                 if g.key(w) == key:
                     fn(x, out=out, stream=s)
+            if timeline is not None:
+                timeline[("reduced", key)] = g.event()
+                timeline[("reduced", key)].record(s)
         with torch.cuda.stream(s):
             for (_, _, _, out), oh in zip(g.ops, outs_host):
                 oh.copy_(out, non_blocking=True)
+        if timeline is not None:
+            timeline["landed"] = landed
+            timeline["end"] = g.event()
+            timeline["end"].record(s)
 
+    # one untimed warm-up step, then one untimed step with events after every
+    # copy and every array's reductions: where the step's time goes
     e2e_step()
     torch.cuda.synchronize()
+    tl = {}
+    e2e_step(tl)
+    torch.cuda.synchronize()
+    t0 = tl["start"]
+    timeline, prev = [], 0.0
+    for key in order:
+        landed_ms = t0.elapsed_time(tl["landed"][key])
+        nbytes = pinned[key].numel() * pinned[key].element_size()
+        timeline.append({"array": "/".join(w.name for w in inputs.SUITE if g.key(w) == key), "bytes": nbytes,
+                         "copy_done_ms": round(landed_ms, 3),
+                         "copy_GBps": round(nbytes / max(landed_ms - prev, 1e-6) / 1e6, 1),
+                         "reduced_ms": round(t0.elapsed_time(tl[("reduced", key)]), 3)})
+        prev = landed_ms
+    end_ms = t0.elapsed_time(tl["end"])
+    timeline_summary = {"per_array": timeline, "step_ms": round(end_ms, 3),
+                        "after_last_copy_ms": round(end_ms - prev, 3)}
     barrier(world)
     ea, eb = g.event(), g.event()
     ea.record(s)
@@ -601,7 +629,8 @@ def measure_e2e(g: Gb300, per_config, steps, world):
     secs = max_over_ranks(world, ea.elapsed_time(eb) / 1e3)
     return {"value": round(step_bytes() * steps * world / secs / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "h2d_GBps": round(h2d * steps / secs / 1e9, 1)}, [oh.numpy().copy() for oh in outs_host]
+            "h2d_GBps": round(h2d * steps / secs / 1e9, 1), "timeline": timeline_summary}, \
+        [oh.numpy().copy() for oh in outs_host]
 
 
 # ---------------------------------------------------------------------------

@@ -106,6 +106,25 @@ int main(void) {
     CHECK_CUDA(cudaMemcpyAsync(&got_b, dbsum, sizeof(float), cudaMemcpyDeviceToHost, s));
     CHECK_RDX(rdx_reduce_ws(RDX_OP_SUM_SUMSQ_F32, df, n, dout, ws, rdx_workspace_bytes(), s));
     CHECK_CUDA(cudaMemcpyAsync(pair, dout, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    /* the same sums split over 3 ranks, each chunk on this GPU, then the rank-order combine */
+    float *dpf, *dcf;
+    int64_t *dpi, *dci;
+    CHECK_CUDA(cudaMalloc((void**)&dpf, 3 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dcf, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dpi, 3 * sizeof(int64_t)));
+    CHECK_CUDA(cudaMalloc((void**)&dci, sizeof(int64_t)));
+    for (int rank = 0; rank < 3; ++rank) {
+        int64_t lo = -1, hi = -1;
+        CHECK_RDX(rdx_shard_range(n, 3, rank, 4, &lo, &hi));
+        CHECK_RDX(rdx_sum_f32(df + lo, hi - lo, dpf + rank, s));
+        CHECK_RDX(rdx_sum_i32_i64(di + lo, hi - lo, dpi + rank, s));
+    }
+    CHECK_RDX(rdx_combine_f32(dpf, 3, dcf, s));
+    CHECK_RDX(rdx_combine_i64(dpi, 3, dci, s));
+    float got_split_f = 0.f;
+    int64_t got_split_i = 0;
+    CHECK_CUDA(cudaMemcpyAsync(&got_split_f, dcf, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_split_i, dci, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
     CHECK_CUDA(cudaStreamSynchronize(s));
 
     int bad = 0;
@@ -123,6 +142,12 @@ int main(void) {
         double e = 0.0;
         for (int64_t j = 0; j < cols; ++j) e += (double)hf[row * cols + j];
         if ((double)got_rows[row] != e) { fprintf(stderr, "row %lld: %.1f != %.1f\n", (long long)row, got_rows[row], e); bad = 1; }
+    }
+    if ((double)got_split_f != sum_f) { fprintf(stderr, "split sum %.1f != %.1f\n", got_split_f, sum_f); bad = 1; }
+    if (got_split_i != sum_i) { fprintf(stderr, "split int sum %lld\n", (long long)got_split_i); bad = 1; }
+    if (rdx_reduce_kernels(RDX_OP_SUM_F32, n) != 1 || rdx_reduce_kernels(RDX_OP_SUM_F32, (int64_t)1 << 28) != 2) {
+        fprintf(stderr, "kernel counts\n");
+        bad = 1;
     }
     /* argument errors come back as statuses, nothing is enqueued */
     if (rdx_sum_f32(df, -1, dout, s) != RDX_ERR_INVALID_ARG) bad = 1;

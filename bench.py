@@ -322,7 +322,7 @@ def config_block():
         "workload": "rdx suite: fp32 sum+sumsq n=2^24+13 N(0,1) s1; int32->int64 sum n=2^28 U{-2^20..2^20} s2; "
                     "fp32 rowsum 8192x32768 and 1048576x256 U[-1,1) s3; bf16->fp32 sum+sumsq n=2^30+7 N(0,1) s4",
         "bytes_read_per_step": step_bytes(),
-        "launches_per_step": len(inputs.SUITE),
+        "calls_per_step": len(inputs.SUITE),
         "l2": f"flushed before every timed launch ({FLUSH_BYTES >> 20} MiB write then {FLUSH_BYTES >> 20} MiB read, "
               "untimed)",
     }

@@ -14,10 +14,12 @@
  *  - Pointers are device pointers (memory the current CUDA device can read
  *    and write: cudaMalloc, torch CUDA tensors, managed memory).  The caller
  *    owns the input and the output buffers.
- *  - Every call is asynchronous: it validates its arguments, enqueues one
- *    kernel on `stream` and returns.  The result is valid in stream order.
- *    `stream` must belong to the current CUDA device; 0 is the legacy default
- *    stream.
+ *  - Every call is asynchronous: it validates its arguments, enqueues its
+ *    kernels on `stream` (one, or two for inputs of 64 MiB and up:
+ *    rdx_reduce_kernels / rdx_rowsum_kernels say which) and returns.  The
+ *    result is valid in stream order.  `stream` must belong to the current
+ *    CUDA device; 0 is the legacy default stream.  (rdx_shard_range and the
+ *    size queries run on the host only.)
  *  - Sizes are element counts (int64_t); no size limit beyond device memory.
  *  - Any element-aligned input pointer is accepted; 16-byte alignment is not
  *    required.  The output must not overlap the input.

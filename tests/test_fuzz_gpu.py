@@ -77,3 +77,36 @@ def test_random_maxima(case):
     z = inputs.integers_i32(n, seed=case, lo=-(2 ** 31), hi=2 ** 31 - 1)
     assert abi.rdx_max_f32(to_device(f, offset)).item() == oracle.max_f32(f)
     assert abi.rdx_max_i32(to_device(z, offset)).item() == oracle.max_i32(z)
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_large_scalar_sizes(case):
+    """Sizes of 64-256 MiB, where the tiles' partials are added by the
+    separate finish kernel (tiles of 64 KiB and more)."""
+    rng = np.random.default_rng(7000 + case)
+    op = OPS[case % len(OPS)]
+    lo_n = (1 << 24) * (2 if "bf16" in op else 1)
+    n = int(math.exp(rng.uniform(math.log(float(lo_n)), math.log(float(1 << 26)))))
+    offset = int(rng.integers(0, VEC[op]))
+    host = host_input(op, n, seed=case)
+    x = to_device(host, offset)
+    assert abi.rdx_reduce_kernels(op, n) == 2
+    got = abi.SCALAR_OPS[op](x).item()
+    check(op, host, got)
+    assert abi.SCALAR_OPS[op](x).item() == got  # the same bits again
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_splits(case):
+    """The sum split into a random number of chunks (as over that many GPUs),
+    emulated on this GPU, against the oracle on the whole array."""
+    from reduction_rdx_sum_gb300 import shard
+
+    rng = np.random.default_rng(11000 + case)
+    op = OPS[case % len(OPS)]
+    n = int(math.exp(rng.uniform(0.0, math.log(float(1 << 23)))))
+    parts = int(rng.integers(1, 81))
+    offset = int(rng.integers(0, VEC[op]))
+    host = host_input(op, n, seed=case)
+    got = shard.emulate(op, to_device(host, offset), parts).item()
+    check(op, host, got)

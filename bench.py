@@ -493,6 +493,34 @@ def measure_extras(g: Gb300, per_config, iters):
     return extras
 
 
+def measure_back_to_back(g: Gb300, steps: int):
+    """The step's seven calls queued back to back, as a pipeline would run
+    them (programmatic dependent launch lets each call start while the one
+    before it drains), one L2 flush before each step and two events around
+    it.  The two calls on the 64 MiB array (smaller than the L2) are kept
+    apart by a 1 GiB and a 2 GiB call, and every other array is larger than
+    the L2, so no call finds its input there.  Context for the headline, which
+    times every call alone after its own flush."""
+    order = ["c2_sum_f32", "c3_sum_i32", "c5_sum_bf16", "c2_sumsq_f32", "c4_rowsum_8192x32768",
+             "c5_sumsq_bf16", "c4_rowsum_1048576x256"]
+    ops = {w.name: (fn, x, out) for (w, fn, x, out) in g.ops}
+    ts = []
+    for it in range(steps + 2):
+        g.flush()
+        e0, e1 = g.event(), g.event()
+        e0.record(g.stream)
+        for name in order:
+            fn, x, out = ops[name]
+            fn(x, out=out, stream=g.stream)
+        e1.record(g.stream)
+        g.torch.cuda.synchronize()
+        if it >= 2:
+            ts.append(e0.elapsed_time(e1))
+    ms = float(np.median(ts))
+    return {"GB/s": round(step_bytes() / (ms * 1e-3) / 1e9, 1), "ms_per_step": round(ms, 4), "steps": steps,
+            "order": order, "l2": "flushed once before each step; the 64 MiB array's two calls 3 GiB apart"}
+
+
 def measure_ladder(g: Gb300, launches=5):
     """The page's five block reductions on a float32 input larger than the
     L2 (config 4's 1 GiB of U[-1,1) values, n = 2^28): the partials alone
@@ -746,6 +774,7 @@ def run_gb300(args):
 
     iters = max(3, min(args.steps, 10))
     extras = measure_extras(g, per_config, iters)
+    back_to_back = measure_back_to_back(g, iters)
     ladder = measure_ladder(g)
     e2e, e2e_results = measure_e2e(g, per_config, max(1, min(args.steps, 20)), world)
 
@@ -778,6 +807,7 @@ def run_gb300(args):
         "gpu_launches": launches_per_step(g) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
+        "step_back_to_back": back_to_back,
         "ladder_fp32_n2^28": ladder,
         "extras": extras,
         "kernel_source_hash": kernel_source_hash(),

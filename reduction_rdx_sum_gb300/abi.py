@@ -59,7 +59,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         for name in ("rdx_sum_f32", "rdx_sumsq_f32", "rdx_sum_bf16_f32acc", "rdx_sumsq_bf16_f32acc",
                      "rdx_sum_i32_i64", "rdx_sum_sumsq_f32", "rdx_sum_sumsq_bf16_f32acc", "rdx_max_f32",
-                     "rdx_max_i32"):
+                     "rdx_max_i32", "rdx_sum_f32_noalloc"):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = [vp, i64, vp, vp], i32
         lib.rdx_rowsum_f32.argtypes, lib.rdx_rowsum_f32.restype = [vp, i64, i64, vp, vp], i32
@@ -301,9 +301,6 @@ def rdx_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None, stream
     """0-d float32 tensor: the sum of a float32 tensor, computed with the
     library's static scratch instead of an allocated workspace (for callers
     that may not allocate device memory; calls must not overlap on the GPU)."""
-    lib = load()
-    fn = lib.rdx_sum_f32_noalloc
-    fn.argtypes, fn.restype = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int
     return _scalar("rdx_sum_f32_noalloc", x, (torch.float32,), torch.float32, out, stream)
 
 

@@ -69,6 +69,23 @@ def local_chunk(op: str, x: torch.Tensor, world: int, rank: int) -> torch.Tensor
     return x.reshape(-1)[lo:hi]
 
 
+def local_partial(op: str, x_local: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """This rank's partial: the one-GPU reduction ``op`` of its chunk."""
+    return _ENTRY[op](x_local, out=out, stream=stream)
+
+
+def combine(op: str, parts: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The gathered partials of ``op`` (rank order along dim 0) added in rank
+    order on the device (rdx_combine_f32, _f32x2 or _i64)."""
+    return _COMBINE[op][0](parts, out=out, stream=stream)
+
+
+def partial_spec(op: str):
+    """(dtype, shape) of one partial of ``op``."""
+    _, dtype, shape = _COMBINE[op]
+    return dtype, shape
+
+
 def gather_partials(partial: torch.Tensor, group=None) -> torch.Tensor:
     """Every rank's ``partial`` stacked in rank order: a (world, *shape)
     tensor on ``partial``'s device, identical on every rank."""
@@ -89,9 +106,7 @@ def sharded_reduce(op: str, x_local: torch.Tensor, group=None, out: torch.Tensor
     (``local_chunk``): the chunk's partial, an all-gather of the partials,
     and their sum in rank order.  Runs on the current CUDA stream; every
     rank returns the same bits."""
-    fn, _, _ = _COMBINE[op]
-    partial = _ENTRY[op](x_local)
-    return fn(gather_partials(partial, group), out=out)
+    return combine(op, gather_partials(local_partial(op, x_local), group), out=out)
 
 
 def sharded_rowsum(x_local_rows: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
@@ -106,11 +121,11 @@ def emulate(op: str, x: torch.Tensor, parts: int, out: torch.Tensor | None = Non
     """The split of ``sharded_reduce`` over ``parts`` ranks, run on one GPU:
     chunk r's partial into slot r of ``partials`` (allocated if None), then
     the combine in rank order.  ``x`` is the whole array."""
-    fn, dtype, shape = _COMBINE[op]
+    dtype, shape = partial_spec(op)
     flat = x.reshape(-1)
     if partials is None:
         partials = torch.empty((parts, *shape), dtype=dtype, device=x.device)
     for r in range(parts):
         lo, hi = shard_range(op, flat.numel(), parts, r)
-        _ENTRY[op](flat[lo:hi], out=partials[r], stream=stream)
-    return fn(partials, out=out, stream=stream)
+        local_partial(op, flat[lo:hi], out=partials[r], stream=stream)
+    return combine(op, partials, out=out, stream=stream)

@@ -134,7 +134,7 @@ def test_emulated_split_matches_the_oracle_on_the_whole_array(op, offset):
         _check_whole(op, host, first)
         assert first.cpu().numpy().tobytes() == again.cpu().numpy().tobytes(), (op, p)
         if p == 1:
-            one = shard._ENTRY[op](x)
+            one = shard.local_partial(op, x)
             assert first.cpu().numpy().tobytes() == one.cpu().numpy().tobytes()
 
 
@@ -147,12 +147,12 @@ def test_chunks_in_their_own_allocations_give_the_emulated_bits(op, p):
     host = _host(op, SIZES[op])
     x = _device(host, 0)
     flat = x.reshape(-1)
-    fn, dtype, shape = shard._COMBINE[op]
+    dtype, shape = shard.partial_spec(op)
     parts = torch.empty((p, *shape), dtype=dtype, device=DEV)
     for r in range(p):
         own = shard.local_chunk(op, flat, p, r).clone()        # a fresh allocation per rank
-        shard._ENTRY[op](own, out=parts[r])
-    got = fn(parts)
+        shard.local_partial(op, own, out=parts[r])
+    got = shard.combine(op, parts)
     emu = shard.emulate(op, x, p)
     torch.cuda.synchronize()
     assert got.cpu().numpy().tobytes() == emu.cpu().numpy().tobytes()

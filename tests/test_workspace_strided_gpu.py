@@ -221,3 +221,37 @@ def test_word_finishing_ops_replay_in_a_cuda_graph(workspace):
         assert outs[0].item() == oracle.sum_i32(zi)
         assert outs[1].item() == oracle.max_i32(zi)
         assert outs[2].item() == oracle.max_f32(zf)
+
+
+def test_two_kernel_calls_replay_in_a_cuda_graph(workspace):
+    # Inputs of 64 MiB and more finish in a second kernel launched behind the
+    # tiles with programmatic dependent launch; a graph of such calls (a
+    # partials finish and a word finish, back to back) keeps both kernels
+    # and their order, replay after replay.
+    n = (1 << 24) + 13
+    assert abi.rdx_reduce_kernels("sum_f32", n) == 2 and abi.rdx_reduce_kernels("sum_i32", n) == 2
+    xf = torch.empty(n, device=DEV)
+    xi = torch.empty(n, dtype=torch.int32, device=DEV)
+    of = torch.empty((), device=DEV)
+    oi = torch.empty((), dtype=torch.int64, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        xf.zero_()
+        xi.zero_()
+        abi.rdx_reduce_ws("sum_f32", xf, workspace, out=of, stream=s)   # warm-up
+        abi.rdx_reduce_ws("sum_i32", xi, workspace, out=oi, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        abi.rdx_reduce_ws("sum_f32", xf, workspace, out=of)
+        abi.rdx_reduce_ws("sum_i32", xi, workspace, out=oi)
+    for seed in (31, 32):
+        hf = inputs.normal_f32(n, seed)
+        hi = inputs.integers_i32(n, seed, -(2 ** 31), 2 ** 31 - 1)
+        xf.copy_(torch.from_numpy(hf))
+        xi.copy_(torch.from_numpy(hi))
+        g.replay()
+        torch.cuda.synchronize()
+        check("sum_f32", hf, of.item())
+        assert oi.item() == oracle.sum_i32(hi)

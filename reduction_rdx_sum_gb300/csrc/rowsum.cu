@@ -353,7 +353,17 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 // only where the reads share a bank at most 2 ways (4 ways for 8 columns or
 // fewer), and rotated reads only up to kRotatedMaxGroups loads per row.  The order depends only on cols, VEC, ROT and, with ROT, the row's
 // lane (its index modulo 32).
-template <int VEC, bool ROT>
+//
+// AD (rows not 16-byte aligned whose starts are 4 words apart modulo 8, or
+// 8 words apart; see rowsum_narrow_read): each row is read as the 16-byte
+// groups of shared memory that cover it, aligned down from its first word,
+// with the words of the first and last group that belong to the neighbouring
+// rows zeroed; four chains, one per word of a group.  Rows 4 (mod 8) words
+// apart put consecutive lanes' groups in alternate halves of the banks, so
+// these wide reads meet no conflict, and a row costs cols / 4 + 1 reads
+// instead of cols.  The order depends on cols and the row's word offset in
+// shared memory (its start modulo 4).
+template <int VEC, bool ROT, bool AD = false>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
                      float* __restrict__ out) {
@@ -394,7 +404,29 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     for (int q = t; q < nr; q += kNarrowBlock) {
         const float* row = tile + s + q * ci;
         float sum;
-        if (ROT) {
+        if (AD) {
+            // words [o, o + ci) of the 16-byte groups starting at the row's
+            // first word rounded down to a group; the last group ends at most
+            // at word kNarrowTile + 4 of the tile (its staged data end at or
+            // before word kNarrowTile + 3), and the words past the row, staged
+            // or not, are zeroed
+            const int start = s + q * ci;
+            const int o = start & 3;
+            const float4* g = reinterpret_cast<const float4*>(tile + (start - o));
+            const int end = o + ci;
+            const int ng = (end + 3) >> 2;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < ng; ++j) {
+                float4 e = g[j];
+                const int w0 = 4 * j;
+                if (w0 + 0 < o || w0 + 0 >= end) e.x = 0.f;
+                if (w0 + 1 < o || w0 + 1 >= end) e.y = 0.f;
+                if (w0 + 2 < o || w0 + 2 >= end) e.z = 0.f;
+                if (w0 + 3 < o || w0 + 3 >= end) e.w = 0.f;
+                a.x += e.x; a.y += e.y; a.z += e.z; a.w += e.w;
+            }
+            sum = (a.x + a.y) + (a.z + a.w);
+        } else if (ROT) {
             // VEC-float groups k0, k0 + 1, ..., wrapping at the row's end
             constexpr int kLanes = kWarpSize;
             const int w = ci / VEC;
@@ -537,7 +569,7 @@ static int narrow_vec(const float* x, int64_t cols) {
 
 // How the narrow kernel reads the rows of a (rows, cols) matrix at x, if it
 // takes them at all.
-enum class NarrowRead { kNo, kPlain, kRotated };
+enum class NarrowRead { kNo, kPlain, kRotated, kAlignedDown };
 
 static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     if (ld != cols || cols <= 0 || cols >= kNarrowMaxCols) return NarrowRead::kNo;
@@ -549,9 +581,17 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
     // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
     const int limit = cols <= 8 ? 4 : 2;
-    if (table.ways[cols][vi][0] <= limit) return NarrowRead::kPlain;
-    if (cols / vec <= kRotatedMaxGroups && table.ways[cols][vi][1] <= limit) return NarrowRead::kRotated;
-    return NarrowRead::kNo;
+    NarrowRead read = NarrowRead::kNo;
+    if (table.ways[cols][vi][0] <= limit) read = NarrowRead::kPlain;
+    else if (cols / vec <= kRotatedMaxGroups && table.ways[cols][vi][1] <= limit) read = NarrowRead::kRotated;
+    // rows not 16-byte aligned, 8 or 4 (mod 8) words apart from 12 up: 16-byte
+    // reads aligned down around each row (measured, 1 GiB: 8 columns 4 bytes
+    // off 210.9 -> 204.8 us, 12 columns 176.1 -> 170.0, 28 columns 12 bytes
+    // off 168.0 -> 157.7, 52 columns 8 bytes off 163.8 -> 157.7; slower at
+    // other widths, where the wide reads meet bank conflicts)
+    if (read != NarrowRead::kNo && vec < 4 && (cols == 8 || (cols % 8 == 4 && cols >= 12)))
+        read = NarrowRead::kAlignedDown;
+    return read;
 }
 
 bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld) {
@@ -567,6 +607,8 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
         const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
         const bool rot = nr == NarrowRead::kRotated;
+        if (nr == NarrowRead::kAlignedDown)
+            return launch_pdl(rowsum_narrow_kernel<1, false, true>, grid, block, stream, x, rows, cols, rpt, out);
         switch (narrow_vec(x, cols)) {
             case 4: return launch_pdl(rowsum_narrow_kernel<4, false>, grid, block, stream, x, rows, cols, rpt, out);
             case 2:

@@ -435,6 +435,18 @@ const char* rdx_last_cuda_error(void);
 /* Free every cached workspace.  Call only when no rdx work is in flight. */
 void rdx_shutdown(void);
 
+/*
+ * rdx_release_stream: free the workspace the library keeps for (current
+ * device, `stream`) (for cudaStreamPerThread: this host thread's), if it has
+ * one; returns 1 if one was freed, 0 if there was none.  For callers that
+ * create and destroy many streams: without it every stream handle that made
+ * a call keeps its workspace (rdx_workspace_bytes()) until rdx_shutdown().
+ * Call it after the stream's rdx work has completed (e.g. after
+ * cudaStreamSynchronize) and before the stream is destroyed; a later call on
+ * the stream allocates a new workspace.  cudaFree may synchronize the device.
+ */
+int rdx_release_stream(cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -87,6 +87,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.rdx_status_string.argtypes, lib.rdx_status_string.restype = [i32], ctypes.c_char_p
         lib.rdx_last_cuda_error.argtypes, lib.rdx_last_cuda_error.restype = [], ctypes.c_char_p
         lib.rdx_shutdown.argtypes, lib.rdx_shutdown.restype = [], None
+        lib.rdx_release_stream.argtypes, lib.rdx_release_stream.restype = [vp], i32
         _lib = lib
         return lib
 
@@ -364,6 +365,16 @@ def rdx_combine_i64(parts: torch.Tensor, out: torch.Tensor | None = None, stream
 
 def rdx_shutdown() -> None:
     load().rdx_shutdown()
+
+
+def rdx_release_stream(stream=None, device=None) -> bool:
+    """Free the library's workspace for ``stream`` (default: the current
+    stream) on ``device`` (default: the current device); True if one was
+    freed.  Call after the stream's work has completed."""
+    index = torch.cuda.current_device() if device is None else torch.device(device).index
+    with torch.cuda.device(index):
+        handle = _current_raw_stream(index) if stream is None else int(stream.cuda_stream)
+        return bool(load().rdx_release_stream(handle))
 
 
 def rdx_debug_build() -> bool:

@@ -428,4 +428,21 @@ void rdx_shutdown(void) {
     g_workspaces.clear();
 }
 
+int rdx_release_stream(cudaStream_t stream) {
+    t_last_error.clear();
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const size_t thread_key =
+        stream == cudaStreamPerThread ? std::hash<std::thread::id>{}(std::this_thread::get_id()) | 1u : 0u;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_workspaces.find(std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), thread_key));
+    if (it == g_workspaces.end()) return 0;
+    cudaFree(it->second);
+    g_workspaces.erase(it);
+    return 1;
+}
+
 }  // extern "C"

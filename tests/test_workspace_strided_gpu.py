@@ -255,3 +255,23 @@ def test_two_kernel_calls_replay_in_a_cuda_graph(workspace):
         torch.cuda.synchronize()
         check("sum_f32", hf, of.item())
         assert oi.item() == oracle.sum_i32(hi)
+
+
+def test_release_stream_frees_and_the_next_call_reallocates():
+    n = (1 << 22) + 5                      # several tiles: the call uses the stream's workspace
+    host = host_input("sum_f32", n, seed=41)
+    x = to_device(host)
+    s = torch.cuda.Stream(DEV)
+    first = abi.rdx_sum_f32(x, stream=s)
+    s.synchronize()
+    assert abi.rdx_release_stream(s) is True
+    assert abi.rdx_release_stream(s) is False       # nothing left to free
+    again = abi.rdx_sum_f32(x, stream=s)             # a fresh workspace, the same bits
+    s.synchronize()
+    assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    check("sum_f32", host, again.item())
+    assert abi.rdx_release_stream(s) is True
+    small = abi.rdx_sum_f32(x[:1000], stream=s)      # one tile: no workspace needed
+    s.synchronize()
+    assert abi.rdx_release_stream(s) is False
+    check("sum_f32", host[:1000], small.item())

@@ -35,7 +35,8 @@
  *    different stream in each).  A workspace is found by the stream's handle:
  *    synchronize a stream before destroying it, or a new stream that is
  *    given the same handle could share the workspace with work still
- *    pending.  rdx_shutdown() frees the library's workspaces.
+ *    pending.  rdx_shutdown() frees the library's workspaces,
+ *    rdx_release_stream() one stream's.
  *  - Errors: no exception crosses this ABI.  Each call returns an rdx_status;
  *    argument errors are found before any CUDA call and nothing is enqueued.
  *    After RDX_ERR_CUDA, rdx_last_cuda_error() names the failing CUDA call.

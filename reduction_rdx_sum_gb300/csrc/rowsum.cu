@@ -581,6 +581,13 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
     // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
     const int limit = cols <= 8 ? 4 : 2;
+    // measured over 33-63 columns at every base offset (1 GiB each): the
+    // short-row kernel is faster for rows read one float at a time whose
+    // width is 2 (mod 4) from 50 up (50 columns 4 bytes off 165.9 -> 159.7 us,
+    // 58 columns 163.8 -> 155.7, 62 columns 165.9 -> 153.6), and for 60
+    // columns off 16-byte alignment
+    if (vec == 1 && cols % 4 == 2 && cols >= 50) return NarrowRead::kNo;
+    if (vec < 4 && cols == 60) return NarrowRead::kNo;
     NarrowRead read = NarrowRead::kNo;
     if (table.ways[cols][vi][0] <= limit) read = NarrowRead::kPlain;
     else if (cols / vec <= kRotatedMaxGroups && table.ways[cols][vi][1] <= limit) read = NarrowRead::kRotated;

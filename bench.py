@@ -546,7 +546,7 @@ def measure_ladder(g: Gb300, launches=5):
     return ladder
 
 
-def measure_sharded(g: Gb300, refs, world, rank, iters):
+def measure_sharded(g: Gb300, refs, world, rank, iters, workloads=(inputs.CFG5_SUM_BF16, inputs.CFG3_SUM_I32)):
     """With several ranks: the bf16 sum (2^30 + 7) and the int32 sum (2^28)
     split over the ranks (strong scaling): each rank reduces its chunk, the
     partials are all-gathered over NCCL and combined in rank order.  Time per
@@ -556,7 +556,7 @@ def measure_sharded(g: Gb300, refs, world, rank, iters):
 
     torch = g.torch
     out = {}
-    for w in (inputs.CFG5_SUM_BF16, inputs.CFG3_SUM_I32):
+    for w in workloads:
         x_local = shard.local_chunk(w.op, g.dev_arrays[g.key(w)], world, rank)
         res = shard.sharded_reduce(w.op, x_local)
         ts = []

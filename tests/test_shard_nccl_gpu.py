@@ -5,8 +5,10 @@ world of one: reduction_rdx_sum_gb300.shard.sharded_reduce takes the rank's
 chunk (the whole array), its partial on the device, an NCCL all-gather of one
 partial into a device array, and the rank-order combine.  Nothing waits on
 another rank.  The result must equal the one-chunk emulation bit for bit and
-the oracle (int exact, floats in tolerance).  Runs in a child process, so the
-test session keeps no process group.
+the oracle (int exact, floats in tolerance).  The bench's own sharded
+measurement then runs on the same process group, on small workloads of the
+bench's recipes, and must report every result matching the oracle.  Runs in
+a child process, so the test session keeps no process group.
 """
 import os
 import socket
@@ -48,6 +50,37 @@ for op, host in cases.items():
         assert abs(v[0] - oracle.sum_bf16(host)) <= 4e-6 * oracle.abssum_bf16(host)
         q = oracle.sumsq_bf16(host)
         assert abs(v[1] - q) <= 4e-6 * q
+
+# the bench's own sharded measurement on the same process group, on small
+# workloads of the same recipes
+import bench
+from reduction_rdx_sum_gb300.runop import L2Flush
+
+class Small:
+    torch = torch
+    stream = torch.cuda.current_stream(dev)
+    def __init__(self):
+        self.flush = L2Flush(dev, 64 << 20)
+        self.dev_arrays = {}
+    @staticmethod
+    def key(w):
+        return (w.dist, w.seed, w.numel)
+    def event(self):
+        return torch.cuda.Event(enable_timing=True)
+
+small = [inputs.Workload("s_bf16", "sum_bf16", ((1 << 22) + 7,), "N(0,1)->bf16", 4),
+         inputs.Workload("s_i32", "sum_i32", ((1 << 22) + 3,), "Z[-1048576,1048576]", 2)]
+g = Small()
+arrays = {}
+for w in small:
+    h = inputs.make(w).reshape(-1)
+    arrays[w.name] = h
+    g.dev_arrays[g.key(w)] = torch.from_numpy(h.view(np.int16) if h.dtype == np.uint16 else h).to(dev)
+refs = {"s_bf16": (oracle.sum_bf16(arrays["s_bf16"]), 4e-6 * oracle.abssum_bf16(arrays["s_bf16"]) + 1e-30),
+        "s_i32": (oracle.sum_i32(arrays["s_i32"]), 0)}
+res = bench.measure_sharded(g, refs, dist.get_world_size(), dist.get_rank(), 3, workloads=small)
+assert set(res) == {"s_bf16_split1", "s_i32_split1"}, res
+assert all(v["parity_ok"] and v["ranks"] == 1 and v["us"] > 0 for v in res.values()), res
 dist.destroy_process_group()
 print("nccl split ok")
 """

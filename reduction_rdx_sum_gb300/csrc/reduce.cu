@@ -24,7 +24,10 @@
 //     and no float atomics are used.  The reductions whose result has the
 //     same bits in any order (the int64 sum and both maxima) fold each block
 //     total into one accumulator word with an integer atomic instead, and
-//     the last block only reads that word back.
+//     the last block only reads that word back.  With tiles of 64 KiB and
+//     more the same pass (or the word's read) runs in finish_kernel, a
+//     second kernel launched behind the tiles, and no tile block waits for a
+//     ticket: the same bits, less tail where the tiles run many waves.
 // Launched with programmatic dependent launch, a call queued behind another
 // kernel is scheduled while that kernel drains and starts reading once its
 // writes are visible.

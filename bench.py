@@ -493,6 +493,13 @@ def measure_extras(g: Gb300, per_config, iters):
     return extras
 
 
+# The step's calls in the order the back-to-back measurement queues them:
+# two calls on one array are kept at least L2_APART_BYTES of other reads apart.
+BACK_TO_BACK_ORDER = ("c2_sum_f32", "c3_sum_i32", "c5_sum_bf16", "c2_sumsq_f32", "c4_rowsum_8192x32768",
+                      "c5_sumsq_bf16", "c4_rowsum_1048576x256")
+L2_APART_BYTES = 1 << 30   # well past the GB300's 129 MB L2
+
+
 def measure_back_to_back(g: Gb300, steps: int):
     """The step's seven calls queued back to back, as a pipeline would run
     them (programmatic dependent launch lets each call start while the one
@@ -501,8 +508,7 @@ def measure_back_to_back(g: Gb300, steps: int):
     apart by a 1 GiB and a 2 GiB call, and every other array is larger than
     the L2, so no call finds its input there.  Context for the headline, which
     times every call alone after its own flush."""
-    order = ["c2_sum_f32", "c3_sum_i32", "c5_sum_bf16", "c2_sumsq_f32", "c4_rowsum_8192x32768",
-             "c5_sumsq_bf16", "c4_rowsum_1048576x256"]
+    order = list(BACK_TO_BACK_ORDER)
     ops = {w.name: (fn, x, out) for (w, fn, x, out) in g.ops}
     ts = []
     for it in range(steps + 2):

@@ -55,3 +55,18 @@ def test_steps_that_differ_in_one_bit_fail():
 def test_nan_fails():
     rep = bench.parity_report(OPS, REFS, [step(float("nan"))], "test")
     assert not rep["s"]["ok"]
+
+
+def test_back_to_back_order_keeps_shared_arrays_apart():
+    """The back-to-back step runs every call once, and two calls on the same
+    array (same recipe) have at least L2_APART_BYTES of other calls' reads
+    between them, so the second cannot find its input in the L2."""
+    by_name = {w.name: w for w in inputs.SUITE}
+    order = list(bench.BACK_TO_BACK_ORDER)
+    assert sorted(order) == sorted(by_name)
+    key = {n: (by_name[n].dist, by_name[n].seed, by_name[n].numel) for n in order}
+    for i, a in enumerate(order):
+        for j in range(i + 1, len(order)):
+            if key[order[j]] == key[a]:
+                between = sum(by_name[n].bytes_read for n in order[i + 1:j])
+                assert between >= bench.L2_APART_BYTES, (a, order[j], between)

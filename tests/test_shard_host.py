@@ -144,3 +144,23 @@ def test_exchange_with_gloo_ranks(lib, world):
     m = inputs.uniform_f32(37 * 129, seed=3, lo=-1.0, hi=1.0).reshape(37, 129)
     rows = np.concatenate([np.array(res[r]["rows"]) for r in range(world)])
     assert np.array_equal(rows, oracle.rowsum_f32(m))
+
+
+def test_chunks_tile_the_range_for_random_arguments(lib):
+    """Property check over random (n, parts, granule): contiguous chunks that
+    tile [0, n), whole granules except the last chunk's tail, balanced."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = hypothesis.strategies
+
+    @hypothesis.settings(max_examples=200, deadline=None)
+    @hypothesis.given(n=st.integers(0, 1 << 40), parts=st.integers(1, 1024), granule=st.sampled_from([1, 2, 4, 8, 16]))
+    def check(n, parts, granule):
+        chunks = [abi.rdx_shard_range(n, parts, r, granule) for r in range(parts)]
+        assert chunks[0][0] == 0 and chunks[-1][1] == n
+        assert all(hi == lo2 for (_, hi), (lo2, _) in zip(chunks, chunks[1:]))
+        assert all(lo % granule == 0 and lo <= hi for lo, hi in chunks)
+        assert all(hi % granule == 0 for _, hi in chunks[:-1])
+        counts = [(hi - lo) // granule for lo, hi in chunks]
+        assert max(counts) - min(counts) <= 1 and counts == sorted(counts, reverse=True)
+
+    check()

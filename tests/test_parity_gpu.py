@@ -181,6 +181,13 @@ def test_overflow_gives_infinity():
     assert abi.rdx_sum_f32(to_device(x)).item() == math.inf
     assert abi.rdx_sum_f32(to_device(-x)).item() == -math.inf
     assert abi.rdx_sumsq_f32(to_device(np.full(n, np.float32(1e17), np.float32))).item() == math.inf
+    # the one-pass pair: the sum stays finite while the sum of squares overflows
+    y = inputs.normal_f32(n, seed=9) * np.float32(1e20)  # sum of squares about 1e46
+    pair = abi.rdx_sum_sumsq_f32(to_device(y, 1)).cpu().numpy().astype(np.float64)
+    assert abs(pair[0] - oracle.sum_f32(y)) <= 1e-6 * oracle.abssum_f32(y) and pair[1] == math.inf
+    yb = np.full(n, 0x5F80, np.uint16)                    # bfloat16 2^64: squares 2^128 pass the float32 range
+    pair = abi.rdx_sum_sumsq_bf16_f32acc(to_device(yb, 3)).cpu().numpy().astype(np.float64)
+    assert pair[0] == n * 2.0 ** 64 and pair[1] == math.inf
     rows = np.full(4 * 65536, np.float32(1e34), np.float32)  # each row's exact sum 6.6e38
     assert abi.rdx_rowsum_f32(to_device(rows).view(4, 65536)).tolist() == [math.inf] * 4
 

@@ -110,3 +110,28 @@ def test_random_splits(case):
     host = host_input(op, n, seed=case)
     got = shard.emulate(op, to_device(host, offset), parts).item()
     check(op, host, got)
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_pairs(case):
+    """The one-pass [sum, sum of squares] pairs over random sizes, offsets and
+    scales.  At scale 1e20 every square passes the float32 range, so the sum
+    of squares is +Inf (the correctly rounded float32 result) while the sum
+    stays finite; at 1e-30 the squares underflow to zero or subnormals."""
+    rng = np.random.default_rng(13000 + case)
+    n = max(1, int(math.exp(rng.uniform(0.0, math.log(float(1 << 23))))))
+    offset = int(rng.integers(0, 4))
+    scale = np.float32(rng.choice([1e-30, 1.0, 1e20]))
+    f = inputs.normal_f32(n, seed=case) * scale
+    s, q = abi.rdx_sum_sumsq_f32(to_device(f, offset)).cpu().numpy().astype(np.float64)
+    assert abs(s - oracle.sum_f32(f)) <= 1e-6 * oracle.abssum_f32(f) + 1e-30
+    if scale == np.float32(1e20):
+        assert q == math.inf
+    else:
+        ref = oracle.sumsq_f32(f)
+        assert abs(q - ref) <= 1e-6 * ref + 1e-30
+    b = inputs.normal_bf16_bits(n, seed=case)
+    s, q = abi.rdx_sum_sumsq_bf16_f32acc(to_device(b, int(rng.integers(0, 8)))).cpu().numpy().astype(np.float64)
+    assert abs(s - oracle.sum_bf16(b)) <= 4e-6 * oracle.abssum_bf16(b) + 1e-30
+    ref = oracle.sumsq_bf16(b)
+    assert abs(q - ref) <= 4e-6 * ref + 1e-30

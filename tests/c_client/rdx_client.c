@@ -1,6 +1,8 @@
 /* A plain C11 client of librdx.so: device memory from the CUDA runtime, no
- * C++ and no PyTorch.  Checks a few entry points against closed forms
- * (inputs are small integers, so every float sum is exact). */
+ * C++ and no PyTorch.  Calls every entry point of rdx.h at least once and
+ * checks the results against closed forms and host sums (inputs are small
+ * integers, so every float sum is exact; the sums of squares pass 2^24 and
+ * are compared within 1e-6 relative). */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -149,6 +151,82 @@ int main(void) {
         fprintf(stderr, "kernel counts\n");
         bad = 1;
     }
+
+    /* every other compute entry point once: sums of squares, the one-pass
+     * pairs, strided rows, a ladder version's partials, the pair combine, the
+     * static-scratch sum, the bank probe and the checked-build counter */
+    const double sumsq = 91.0 * (double)q + (double)((r - 1) * r * (2 * r - 1) / 6); /* 0^2 + ... + 6^2 = 91 */
+    const int64_t cols_s = 4000, ld = 4099;  /* rows * ld < n */
+    const int64_t nl1 = rdx_ladder_num_partials(1, n);
+    float *dsq, *dsqb, *dp2, *dp2b, *dstr, *dl1, *dpp, *dcp, *dna;
+    int64_t* dcycles;
+    uint32_t* dsink;
+    CHECK_CUDA(cudaMalloc((void**)&dsq, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dsqb, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dp2, 2 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dp2b, 2 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dstr, (size_t)rows * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dl1, (size_t)nl1 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dpp, 3 * 2 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dcp, 2 * sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dna, sizeof(float)));
+    CHECK_CUDA(cudaMalloc((void**)&dcycles, sizeof(int64_t)));
+    CHECK_CUDA(cudaMalloc((void**)&dsink, 32 * sizeof(uint32_t)));
+    CHECK_RDX(rdx_sumsq_f32(df, n, dsq, s));
+    CHECK_RDX(rdx_sumsq_bf16_f32acc(db, n, dsqb, s));
+    CHECK_RDX(rdx_sum_sumsq_f32(df, n, dp2, s));
+    CHECK_RDX(rdx_sum_sumsq_bf16_f32acc(db, n, dp2b, s));
+    CHECK_RDX(rdx_rowsum_strided_f32(df, rows, cols_s, ld, dstr, s));
+    CHECK_RDX(rdx_ladder_partials_f32(1, df, n, dl1, s));
+    for (int rank = 0; rank < 3; ++rank) {
+        int64_t lo = -1, hi = -1;
+        CHECK_RDX(rdx_shard_range(n, 3, rank, 4, &lo, &hi));
+        CHECK_RDX(rdx_sum_sumsq_f32(df + lo, hi - lo, dpp + 2 * rank, s));
+    }
+    CHECK_RDX(rdx_combine_f32x2(dpp, 3, dcp, s));
+    CHECK_RDX(rdx_sum_f32_noalloc(df, n, dna, s));
+    CHECK_RDX(rdx_bank_probe(0, 16, dcycles, dsink, s));
+    float got_sq = 0.f, got_sqb = 0.f, p2[2] = {0.f, 0.f}, p2b[2] = {0.f, 0.f}, cp[2] = {0.f, 0.f}, got_na = 0.f;
+    int64_t cycles = 0;
+    float* got_str = (float*)malloc((size_t)rows * sizeof(float));
+    float* got_l1 = (float*)malloc((size_t)nl1 * sizeof(float));
+    if (!got_str || !got_l1) return 4;
+    CHECK_CUDA(cudaMemcpyAsync(&got_sq, dsq, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_sqb, dsqb, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(p2, dp2, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(p2b, dp2b, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(got_str, dstr, (size_t)rows * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(got_l1, dl1, (size_t)nl1 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(cp, dcp, 2 * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&got_na, dna, sizeof(float), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaMemcpyAsync(&cycles, dcycles, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+    CHECK_CUDA(cudaStreamSynchronize(s));
+    /* the sums of squares pass 2^24, so float32 partial sums round: compare within 1e-6 relative */
+    const double sq_tol = 1e-6 * sumsq;
+    if (got_sq - sumsq > sq_tol || sumsq - got_sq > sq_tol) { fprintf(stderr, "sumsq_f32 %.1f\n", got_sq); bad = 1; }
+    if (got_sqb - sumsq > sq_tol || sumsq - got_sqb > sq_tol) { fprintf(stderr, "sumsq_bf16 %.1f\n", got_sqb); bad = 1; }
+    if ((double)p2[0] != sum_f || p2[1] - sumsq > sq_tol || sumsq - p2[1] > sq_tol) { fprintf(stderr, "pair f32\n"); bad = 1; }
+    if ((double)p2b[0] != sum_f || p2b[1] - sumsq > sq_tol || sumsq - p2b[1] > sq_tol) { fprintf(stderr, "pair bf16\n"); bad = 1; }
+    if ((double)cp[0] != sum_f || cp[1] - sumsq > sq_tol || sumsq - cp[1] > sq_tol) { fprintf(stderr, "split pair\n"); bad = 1; }
+    for (int64_t row = 0; row < rows && !bad; ++row) {
+        double e = 0.0;
+        for (int64_t j = 0; j < cols_s; ++j) e += (double)hf[row * ld + j];
+        if ((double)got_str[row] != e) { fprintf(stderr, "strided row %lld\n", (long long)row); bad = 1; }
+    }
+    for (int64_t b = 0; b < nl1 && !bad; ++b) {
+        double e = 0.0;
+        for (int64_t i = b * 256; i < n && i < (b + 1) * 256; ++i) e += (double)hf[i];
+        if ((double)got_l1[b] != e) { fprintf(stderr, "ladder v1 partial %lld\n", (long long)b); bad = 1; }
+    }
+    if (memcmp(&got_na, &got_f, sizeof(float)) != 0) { fprintf(stderr, "static-scratch sum %.1f\n", got_na); bad = 1; }
+    if (cycles <= 0 || rdx_bank_probe_loads_per_iter() < 1) { fprintf(stderr, "bank probe\n"); bad = 1; }
+    if (rdx_rowsum_kernels(rows, cols) < 1 || rdx_combine_max_parts() != 4096) { fprintf(stderr, "queries\n"); bad = 1; }
+    uint64_t violations = 1;
+    CHECK_RDX(rdx_debug_violations(&violations, 0));
+    if (rdx_debug_build() != 0 || violations != 0) { fprintf(stderr, "normal build\n"); bad = 1; }
+    /* the stream made calls, so it holds a workspace; releasing it twice frees it once */
+    if (rdx_release_stream(s) != 1 || rdx_release_stream(s) != 0) { fprintf(stderr, "release stream\n"); bad = 1; }
+
     /* argument errors come back as statuses, nothing is enqueued */
     if (rdx_sum_f32(df, -1, dout, s) != RDX_ERR_INVALID_ARG) bad = 1;
     if (rdx_sum_f32(df, n, (float*)(df + 8), s) != RDX_ERR_INVALID_ARG) bad = 1;

@@ -195,7 +195,9 @@ rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t s
  *   cols  >= 0; cols == 0 writes rows zeros
  *   out   rows float32 values; must not overlap x
  * Rows of fewer than 64 columns (contiguous) are staged through shared
- * memory in tiles of whole rows and summed one row per thread; short and
+ * memory in tiles of whole rows and summed one row per thread (where those
+ * reads would meet shared-memory bank conflicts, each tile arrives by one
+ * bulk copy whose barrier wait is bounded: see rdx_wait_timeouts); short and
  * medium rows are summed by a group of threads each, long rows by a block
  * each, with no workspace.  Few, very long rows (fewer than two waves of
  * blocks, at least 16384 columns, at most 2048 rows) are each cut into tiles
@@ -425,6 +427,30 @@ int rdx_bank_probe_loads_per_iter(void);
  */
 int rdx_debug_build(void);
 rdx_status rdx_debug_violations(uint64_t* count, int reset);
+
+/*
+ * Bounded waits.  The narrow-row kernel of rdx_rowsum_f32 (rows of fewer
+ * than 64 columns whose shared-memory reads would share a bank) stages each
+ * tile with one bulk copy and waits on a shared-memory barrier for its bytes.
+ * A wait that has not completed after one second (the GPU's global timer)
+ * gives up: the block counts one timeout, waits once more (bounded) for its
+ * copy to land, and exits without writing its rows' sums.  No such wait has
+ * ever been seen to give up on a healthy GPU; a nonzero count means that
+ * some row sums of the calls since the last reset were not written.
+ * rdx_wait_timeouts: *count = those timeouts on the current device since the
+ * last reset; synchronizes the device first; reset != 0 clears the count.
+ * Errors: RDX_ERR_INVALID_ARG if count is NULL; RDX_ERR_CUDA if the device
+ * or the counter cannot be read.
+ * rdx_debug_stage_timeout: test hook for that path.  Enqueues one tile of
+ * `rows` rows of `cols` floats (0 < cols < 64, 0 < rows * cols <= 6144, x
+ * 16-byte aligned and holding at least 4 floats) whose barrier is armed for
+ * 16 bytes more than its copy brings, so that its wait gives up after one
+ * second: the count rises by one and out is not written.  Errors:
+ * RDX_ERR_INVALID_ARG for arguments outside those limits, NULL pointers or
+ * overlap; RDX_ERR_CUDA if the launch fails.
+ */
+rdx_status rdx_wait_timeouts(uint64_t* count, int reset);
+rdx_status rdx_debug_stage_timeout(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream);
 
 /* Static text for a status code ("ok", "invalid argument", ...). */
 const char* rdx_status_string(rdx_status status);

@@ -74,6 +74,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.rdx_bank_probe_loads_per_iter.argtypes, lib.rdx_bank_probe_loads_per_iter.restype = [], i32
         lib.rdx_debug_build.argtypes, lib.rdx_debug_build.restype = [], i32
         lib.rdx_debug_violations.argtypes, lib.rdx_debug_violations.restype = [vp, i32], i32
+        lib.rdx_wait_timeouts.argtypes, lib.rdx_wait_timeouts.restype = [vp, i32], i32
+        lib.rdx_debug_stage_timeout.argtypes, lib.rdx_debug_stage_timeout.restype = [vp, i64, i64, vp, vp], i32
         lib.rdx_ladder_partials_f32.argtypes = [i32, vp, i64, vp, vp]
         lib.rdx_ladder_partials_f32.restype = i32
         lib.rdx_ladder_num_partials.argtypes, lib.rdx_ladder_num_partials.restype = [i32, i64], i64
@@ -387,6 +389,25 @@ def rdx_debug_violations(reset: bool = False) -> int:
     count = ctypes.c_uint64(0)
     _check("rdx_debug_violations", load().rdx_debug_violations(ctypes.byref(count), int(reset)))
     return int(count.value)
+
+
+def rdx_wait_timeouts(reset: bool = False) -> int:
+    """Staging waits of the narrow-row kernel that gave up on the current
+    device since the last reset (synchronizes the device)."""
+    count = ctypes.c_uint64(0)
+    _check("rdx_wait_timeouts", load().rdx_wait_timeouts(ctypes.byref(count), int(reset)))
+    return int(count.value)
+
+
+def rdx_debug_stage_timeout(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Test hook: one narrow-row tile of the 2-D float32 tensor x (rows *
+    cols <= 6144) whose staging wait cannot complete, so that it gives up
+    after one second; out (rows float32 values) is left unwritten."""
+    if x.dim() != 2 or x.dtype != torch.float32 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous 2-D float32 CUDA tensor")
+    rows, cols = x.shape
+    _check("rdx_debug_stage_timeout",
+           _launch(load().rdx_debug_stage_timeout, x.device, stream, x.data_ptr(), rows, cols, out.data_ptr()))
 
 
 # Entry points by operation name, for the tests and the bench.

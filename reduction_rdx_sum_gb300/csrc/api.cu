@@ -409,6 +409,35 @@ rdx_status rdx_debug_violations(uint64_t* count, int reset) {
     return RDX_OK;
 }
 
+rdx_status rdx_wait_timeouts(uint64_t* count, int reset) {
+    t_last_error.clear();
+    if (count == nullptr) return RDX_ERR_INVALID_ARG;
+    *count = 0;
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceSynchronize", e);
+    const unsigned long long v = rdx::rowsum_stage_timeouts(reset != 0);
+    if (v == ~0ull) {
+        t_last_error = "cudaMemcpyFromSymbol of the staging-timeout counter failed";
+        return RDX_ERR_CUDA;
+    }
+    *count = v;
+    return RDX_OK;
+}
+
+rdx_status rdx_debug_stage_timeout(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
+    t_last_error.clear();
+    if (x == nullptr || out == nullptr || cols <= 0 || cols >= 64 || rows <= 0 || rows > 6144 ||
+        rows * cols > 6144 || rows * cols < 4 || !is_aligned(x, 16) || !is_aligned(out, 4))
+        return RDX_ERR_INVALID_ARG;
+    if (overlaps(x, size_t(rows * cols) * 4, out, size_t(rows) * 4)) return RDX_ERR_INVALID_ARG;
+    const DeviceCaps* dev = nullptr;
+    const rdx_status st = current_device(&dev);
+    if (st != RDX_OK) return st;
+    const cudaError_t e = rdx::rowsum_stage_timeout_probe(x, rows, cols, out, stream);
+    if (e != cudaSuccess) return fail_cuda("staging-timeout probe launch", e);
+    return RDX_OK;
+}
+
 const char* rdx_status_string(rdx_status status) {
     switch (status) {
         case RDX_OK: return "ok";

@@ -117,6 +117,12 @@ cudaError_t combine_launch(CombineType type, const void* parts, int p, void* out
 // ---- checked build (RDX_DEBUG=1): out-of-range accesses caught, per file ------
 unsigned long long reduce_out_of_range(bool reset);
 unsigned long long rowsum_out_of_range(bool reset);
+// Staging waits of the narrow-row kernel that gave up on the current device
+// (~0 if the count could not be read); reset clears it.
+unsigned long long rowsum_stage_timeouts(bool reset);
+// Test hook: one narrow-row tile (rows * cols <= 6144 floats, x 16-byte
+// aligned) whose staging wait cannot complete, so that it gives up.
+cudaError_t rowsum_stage_timeout_probe(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream);
 unsigned long long ladder_out_of_range(bool reset);
 unsigned long long shard_out_of_range(bool reset);
 

@@ -54,6 +54,7 @@ constexpr int64_t kFitRowMaxCols = 512;  // 4 vectors x 32 lanes x 4 floats
 constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight together
 constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
 constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
+constexpr int kNarrowBulkTile = 6144;    // the same with bulk-copy staging (24 KiB: 8 blocks per SM)
 constexpr int64_t kNarrowMaxCols = 64;   // narrow rows: fewer columns than this
 // Rotated reads (see rowsum_narrow_kernel) pay one shared load per VEC-float
 // group of a row; measured against the short-row kernel, they win up to 52
@@ -75,6 +76,50 @@ __device__ __forceinline__ void cp_async4(float* smem_dst, const float* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Bulk-copy staging of the narrow kernel.  Thread 0 initialises a shared-
+// memory barrier, arms it for the bytes to come (plus extra, 0 except in the
+// timeout test) and starts one bulk copy (the copy engine of the SM, no
+// thread registers) of `bytes` bytes from global src to shared dst; both
+// addresses and the size are multiples of 16 bytes.  The barrier's phase 0
+// completes when every byte has landed.
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bulk_load(float* dst, const void* src, unsigned bytes, unsigned long long* bar,
+                                          unsigned extra) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes + extra)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// Staging waits that gave up, counted in every build and read (and cleared)
+// by the host through rowsum_stage_timeouts().
+__device__ unsigned long long g_stage_timeouts;
+constexpr unsigned long long kStageWaitNs = 1000000000ull;  // one second of wall time
+
+// Wait for phase 0 of the barrier, for at most kStageWaitNs by the GPU's
+// global timer: true once it has completed, false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar) {
+    const unsigned a = smem_addr(bar);
+    unsigned long long t0 = 0;
+    for (;;) {
+        unsigned done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(a)
+            : "memory");
+        if (done) return true;
+        unsigned long long now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > kStageWaitNs) return false;
+    }
+}
 
 // Sum of lane l's share of one row, the row split among LPR lanes.  With
 // EDGES (the matrix has rows that are not 16-byte aligned) the up to 3 + 3
@@ -363,18 +408,19 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 // these wide reads meet no conflict, and a row costs cols / 4 + 1 reads
 // instead of cols.  The order depends on cols and the row's word offset in
 // shared memory (its start modulo 4).
-template <int VEC, bool ROT, bool AD = false>
+template <int VEC, bool ROT, bool AD, bool BULK>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
-                     float* __restrict__ out) {
+                     float* __restrict__ out, unsigned extra_tx) {
     pdl_wait();     // the previous kernel in the stream has finished writing
     pdl_release();  // the next one may be scheduled into SMs this grid frees
-    __shared__ __align__(16) float tile[kNarrowTile + 4];
+    constexpr int kTile = BULK ? kNarrowBulkTile : kNarrowTile;
+    __shared__ __align__(16) float tile[kTile + 4];
     const int t = threadIdx.x;
     const int ci = int(cols);
     const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
     const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
-    const int len = nr * ci;                          // floats of this tile, <= kNarrowTile
+    const int len = nr * ci;                          // floats of this tile, <= kTile
     const float* __restrict__ p0 = x + r0 * cols;
     const size_t span = size_t(rows) * size_t(cols) * 4;
     int h = int(((16u - (unsigned(reinterpret_cast<uintptr_t>(p0)) & 15u)) & 15u) >> 2);
@@ -384,22 +430,45 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     const int s = -h & 3;                             // tile float i lives at tile[s + i]
     const uint4* __restrict__ pv = reinterpret_cast<const uint4*>(p0 + h);
 
-    constexpr int kLoads = kNarrowTile / 4 / kNarrowBlock;  // vectors per thread, all in flight
-    uint4 v[kLoads];
+    if (BULK) {
+        // one bulk copy of the tile's m vectors, tracked by a shared-memory
+        // barrier (its byte count armed by thread 0 before the copy starts);
+        // extra_tx is 0 except in the timeout test, where it keeps the
+        // barrier from completing
+        __shared__ __align__(8) unsigned long long bar;
+        __shared__ int staged;
+        if (t == 0) {
+            staged = m > 0 && guard(pv, size_t(m) * 16, x, span);
+            if (staged) bulk_load(tile + s + h, pv, unsigned(m) * 16u, &bar, extra_tx);
+        }
+        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
+        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
+        __syncthreads();  // the barrier is armed, the edge floats are stored
+        if (staged && !mbar_wait_bounded(&bar)) {
+            // gave up: count it, let the copy land (a second bounded wait)
+            // before the block's shared memory is released, write nothing
+            if (t == 0) atomicAdd(&g_stage_timeouts, 1ull);
+            (void)mbar_wait_bounded(&bar);
+            return;
+        }
+    } else {
+        constexpr int kLoads = kTile / 4 / kNarrowBlock;  // vectors per thread, all in flight
+        uint4 v[kLoads];
 #pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-        const int k = t + u * kNarrowBlock;
-        v[u] = k < m && guard(pv + k, 16, x, span) ? ld_stream16(pv + k) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    batch_fence(v);
+        for (int u = 0; u < kLoads; ++u) {
+            const int k = t + u * kNarrowBlock;
+            v[u] = k < m && guard(pv + k, 16, x, span) ? ld_stream16(pv + k) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        batch_fence(v);
 #pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-        const int k = t + u * kNarrowBlock;
-        if (k < m) *reinterpret_cast<uint4*>(tile + s + h + 4 * k) = v[u];
+        for (int u = 0; u < kLoads; ++u) {
+            const int k = t + u * kNarrowBlock;
+            if (k < m) *reinterpret_cast<uint4*>(tile + s + h + 4 * k) = v[u];
+        }
+        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
+        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
+        __syncthreads();
     }
-    if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
-    if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
-    __syncthreads();
 
     for (int q = t; q < nr; q += kNarrowBlock) {
         const float* row = tile + s + q * ci;
@@ -407,9 +476,9 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
         if (AD) {
             // words [o, o + ci) of the 16-byte groups starting at the row's
             // first word rounded down to a group; the last group ends at most
-            // at word kNarrowTile + 4 of the tile (its staged data end at or
-            // before word kNarrowTile + 3), and the words past the row, staged
-            // or not, are zeroed
+            // at word kTile + 4 of the tile (its staged data end at or before
+            // word kTile + 3), and the words past the row, staged or not, are
+            // zeroed
             const int start = s + q * ci;
             const int o = start & 3;
             const float4* g = reinterpret_cast<const float4*>(tile + (start - o));
@@ -516,6 +585,24 @@ cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld,
 
 RDX_DEFINE_VIOLATION_COUNTER(rowsum_out_of_range)
 
+unsigned long long rowsum_stage_timeouts(bool reset) {
+    unsigned long long v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_stage_timeouts, sizeof v) != cudaSuccess) return ~0ull;
+    if (reset) {
+        const unsigned long long z = 0;
+        if (cudaMemcpyToSymbol(g_stage_timeouts, &z, sizeof z) != cudaSuccess) return ~0ull;
+    }
+    return v;
+}
+
+cudaError_t rowsum_stage_timeout_probe(const float* x, int64_t rows, int64_t cols, float* out, cudaStream_t stream) {
+    if (cols <= 0 || cols >= kNarrowMaxCols || rows <= 0 || rows > kNarrowBulkTile || rows * cols > kNarrowBulkTile)
+        return cudaErrorInvalidValue;
+    // one tile; its barrier is armed for 16 bytes more than the copy brings
+    return launch_pdl(rowsum_narrow_kernel<1, false, false, true>, dim3(1), dim3(kNarrowBlock), stream, x, rows, cols,
+                      rows, out, 16u);
+}
+
 bool rowsum_use_split(int64_t rows, int64_t cols) {
     // At most kMaxSplitRows rows (fewer than two waves of one block per row
     // on a 152-SM GPU), each long enough for at least four tiles.  The rule
@@ -542,18 +629,46 @@ static int narrow_bank_ways(int cols, int vec, bool rotated) {
     return worst;
 }
 
-// narrow_bank_ways for every narrow width and read width, worked out once.
+// The same figure for the aligned-down reads (AD): lane l's row starts at
+// word s0 + l * cols of the tile (s0 = the tile's staging offset, the same
+// for every row when cols % 4 == 0), and in step j the lane reads 16-byte
+// group j counted from the one holding that word, while its row has one.
+static int narrow_ad_ways(int cols, int s0) {
+    int worst = 0;
+    for (int j = 0; j <= (3 + cols + 3) / 4; ++j) {
+        int count[kWarpSize] = {};
+        for (int lane = 0; lane < kWarpSize; ++lane) {
+            const int start = s0 + lane * cols, o = start & 3;
+            if (j >= (o + cols + 3) / 4) continue;
+            const int g = (start - o) / 4 + j;
+            for (int e = 0; e < 4; ++e) ++count[(4 * g + e) % kWarpSize];
+        }
+        for (int b = 0; b < kWarpSize; ++b) worst = worst > (count[b] + 3) / 4 ? worst : (count[b] + 3) / 4;
+    }
+    return worst;
+}
+
+// narrow_bank_ways and narrow_ad_ways for every narrow width, read width and
+// staging offset, worked out once.
 struct NarrowWays {
     unsigned char ways[kNarrowMaxCols][3][2] = {};  // [cols][vec 1, 2, 4 -> 0, 1, 2][rotated]
+    unsigned char ad[kNarrowMaxCols][4] = {};       // [cols][s0], cols % 4 == 0
     NarrowWays() {
-        for (int c = 1; c < kNarrowMaxCols; ++c)
+        for (int c = 1; c < kNarrowMaxCols; ++c) {
             for (int vi = 0; vi < 3; ++vi) {
                 const int vec = 1 << vi;
                 if (c % vec) continue;
                 for (int r = 0; r < 2; ++r) ways[c][vi][r] = static_cast<unsigned char>(narrow_bank_ways(c, vec, r != 0));
             }
+            if (c % 4 == 0)
+                for (int s0 = 0; s0 < 4; ++s0) ad[c][s0] = static_cast<unsigned char>(narrow_ad_ways(c, s0));
+        }
     }
 };
+static const NarrowWays& narrow_ways() {
+    static const NarrowWays table;
+    return table;
+}
 
 // Shared-memory read width of the narrow kernel.  Rows start every cols
 // words after the tile's staging offset s = (4 - h) % 4, h the floats before
@@ -577,7 +692,7 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     // 16-byte aligned rows of 16, 24, ... columns: the short-row kernel reads
     // them as whole vectors and is faster
     if (vec == 4 && cols % 8 == 0 && cols > 8) return NarrowRead::kNo;
-    static const NarrowWays table;
+    const NarrowWays& table = narrow_ways();
     const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
     // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
     const int limit = cols <= 8 ? 4 : 2;
@@ -601,6 +716,26 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     return read;
 }
 
+// How many ways the chosen reads share a shared-memory bank (1 = no
+// conflict).  Where they share 2 or more, the kernel stages its tiles with
+// one bulk copy instead of per-thread loads (measured over every narrow
+// width at every 4-byte base offset, 1 GiB each: 4 columns 4 bytes off
+// 233 -> 186 us, 8 columns 4-12 bytes off 205 -> 170, even widths 4 or 12
+// bytes off 4-14 us faster, 2-way rotated reads 1-14 us; where the reads do
+// not conflict, per-thread loads are 2-10 us faster and stay).
+static int narrow_read_ways(const float* x, int64_t cols, NarrowRead nr) {
+    const NarrowWays& table = narrow_ways();
+    const int vec = narrow_vec(x, cols);
+    const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
+    switch (nr) {
+        case NarrowRead::kPlain: return table.ways[cols][vi][0];
+        case NarrowRead::kRotated: return table.ways[cols][vi][1];
+        case NarrowRead::kAlignedDown:
+            return table.ad[cols][(reinterpret_cast<uintptr_t>(x) / 4) % 4];
+        default: return 0;
+    }
+}
+
 bool rowsum_use_narrow(const float* x, int64_t cols, int64_t ld) {
     return rowsum_narrow_read(x, cols, ld) != NarrowRead::kNo;
 }
@@ -609,21 +744,47 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
     if (rows <= 0) return cudaSuccess;
     const NarrowRead nr = rowsum_narrow_read(x, cols, ld);
     if (nr != NarrowRead::kNo) {
-        const int64_t rpt = kNarrowTile / cols;  // whole rows per tile
+        const bool bulk = narrow_read_ways(x, cols, nr) >= 2;
+        const int64_t rpt = (bulk ? kNarrowBulkTile : kNarrowTile) / cols;  // whole rows per tile
         const int64_t blocks = (rows + rpt - 1) / rpt;
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
         const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
         const bool rot = nr == NarrowRead::kRotated;
+        const int vec = narrow_vec(x, cols);
+        if (bulk) {
+            if (nr == NarrowRead::kAlignedDown)
+                return launch_pdl(rowsum_narrow_kernel<1, false, true, true>, grid, block, stream, x, rows, cols, rpt,
+                                  out, 0u);
+            if (vec == 4)
+                return launch_pdl(rowsum_narrow_kernel<4, false, false, true>, grid, block, stream, x, rows, cols, rpt,
+                                  out, 0u);
+            if (vec == 2)
+                return rot ? launch_pdl(rowsum_narrow_kernel<2, true, false, true>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u)
+                           : launch_pdl(rowsum_narrow_kernel<2, false, false, true>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u);
+            return rot ? launch_pdl(rowsum_narrow_kernel<1, true, false, true>, grid, block, stream, x, rows, cols, rpt,
+                                    out, 0u)
+                       : launch_pdl(rowsum_narrow_kernel<1, false, false, true>, grid, block, stream, x, rows, cols, rpt,
+                                    out, 0u);
+        }
         if (nr == NarrowRead::kAlignedDown)
-            return launch_pdl(rowsum_narrow_kernel<1, false, true>, grid, block, stream, x, rows, cols, rpt, out);
-        switch (narrow_vec(x, cols)) {
-            case 4: return launch_pdl(rowsum_narrow_kernel<4, false>, grid, block, stream, x, rows, cols, rpt, out);
+            return launch_pdl(rowsum_narrow_kernel<1, false, true, false>, grid, block, stream, x, rows, cols, rpt, out,
+                              0u);
+        switch (vec) {
+            case 4:
+                return launch_pdl(rowsum_narrow_kernel<4, false, false, false>, grid, block, stream, x, rows, cols, rpt,
+                                  out, 0u);
             case 2:
-                return rot ? launch_pdl(rowsum_narrow_kernel<2, true>, grid, block, stream, x, rows, cols, rpt, out)
-                           : launch_pdl(rowsum_narrow_kernel<2, false>, grid, block, stream, x, rows, cols, rpt, out);
+                return rot ? launch_pdl(rowsum_narrow_kernel<2, true, false, false>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u)
+                           : launch_pdl(rowsum_narrow_kernel<2, false, false, false>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u);
             default:
-                return rot ? launch_pdl(rowsum_narrow_kernel<1, true>, grid, block, stream, x, rows, cols, rpt, out)
-                           : launch_pdl(rowsum_narrow_kernel<1, false>, grid, block, stream, x, rows, cols, rpt, out);
+                return rot ? launch_pdl(rowsum_narrow_kernel<1, true, false, false>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u)
+                           : launch_pdl(rowsum_narrow_kernel<1, false, false, false>, grid, block, stream, x, rows, cols,
+                                        rpt, out, 0u);
         }
     }
     if (cols <= kFitRowMaxCols) {

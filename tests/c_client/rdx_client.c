@@ -224,6 +224,16 @@ int main(void) {
     uint64_t violations = 1;
     CHECK_RDX(rdx_debug_violations(&violations, 0));
     if (rdx_debug_build() != 0 || violations != 0) { fprintf(stderr, "normal build\n"); bad = 1; }
+    /* the bounded staging wait: no call so far gave up; the test hook's tile
+     * cannot complete, so its wait gives up after a second and is counted */
+    uint64_t timeouts = 1;
+    float* dprobe;
+    CHECK_CUDA(cudaMalloc((void**)&dprobe, 100 * sizeof(float)));
+    CHECK_RDX(rdx_wait_timeouts(&timeouts, 1));
+    if (timeouts != 0) { fprintf(stderr, "timeouts before the probe\n"); bad = 1; }
+    CHECK_RDX(rdx_debug_stage_timeout(df, 100, 16, dprobe, s));
+    CHECK_RDX(rdx_wait_timeouts(&timeouts, 1));
+    if (timeouts != 1) { fprintf(stderr, "probe timeouts %llu\n", (unsigned long long)timeouts); bad = 1; }
     /* the stream made calls, so it holds a workspace; releasing it twice frees it once */
     if (rdx_release_stream(s) != 1 || rdx_release_stream(s) != 0) { fprintf(stderr, "release stream\n"); bad = 1; }
 

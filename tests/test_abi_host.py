@@ -178,3 +178,20 @@ def test_kernel_counts_per_call(lib):
     assert abi.rdx_rowsum_kernels(8192, 32768) == 1 and abi.rdx_rowsum_kernels(1 << 20, 256) == 1
     assert abi.rdx_rowsum_kernels(4, 1 << 26) == 2
     assert abi.rdx_rowsum_kernels(-1, 5) == -1
+
+
+def test_stage_timeout_entry_validation(lib):
+    # every argument check comes before any CUDA call
+    assert lib.rdx_wait_timeouts(None, 0) == INVALID
+    f = lib.rdx_debug_stage_timeout
+    assert f(None, 100, 16, FAKE + 65536, None) == INVALID
+    assert f(FAKE, 100, 16, None, None) == INVALID
+    assert f(FAKE, 100, 0, FAKE + 65536, None) == INVALID              # cols outside 1..63
+    assert f(FAKE, 100, 64, FAKE + 65536, None) == INVALID
+    assert f(FAKE, 0, 16, FAKE + 65536, None) == INVALID               # no rows
+    assert f(FAKE, 385, 16, FAKE + 65536, None) == INVALID             # more than one 6144-float tile
+    assert f(FAKE, 1 << 62, 16, FAKE + 65536, None) == INVALID         # rows far beyond, no overflow
+    assert f(FAKE, 1, 3, FAKE + 65536, None) == INVALID                # fewer than 4 floats
+    assert f(FAKE + 4, 100, 16, FAKE + 65536, None) == INVALID         # x not 16-byte aligned
+    assert f(FAKE, 100, 16, FAKE + 65538, None) == INVALID             # out misaligned
+    assert f(FAKE, 100, 16, FAKE + 64, None) == INVALID                # out inside x

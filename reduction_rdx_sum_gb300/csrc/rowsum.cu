@@ -720,7 +720,7 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
 // conflict).  Where they share 2 or more, the kernel stages its tiles with
 // one bulk copy instead of per-thread loads (measured over every narrow
 // width at every 4-byte base offset, 1 GiB each: 4 columns 4 bytes off
-// 233 -> 186 us, 8 columns 4-12 bytes off 205 -> 170, even widths 4 or 12
+// 231 -> 186 us, 8 columns 4-12 bytes off 205 -> 170, even widths 4 or 12
 // bytes off 4-14 us faster, 2-way rotated reads 1-14 us; where the reads do
 // not conflict, per-thread loads are 2-10 us faster and stay).
 static int narrow_read_ways(const float* x, int64_t cols, NarrowRead nr) {

@@ -194,7 +194,7 @@ rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t s
  *   rows  >= 0; rows == 0 enqueues nothing
  *   cols  >= 0; cols == 0 writes rows zeros
  *   out   rows float32 values; must not overlap x
- * Rows of fewer than 64 columns (contiguous) are staged through shared
+ * Rows of at most 64 columns (contiguous) are staged through shared
  * memory in tiles of whole rows and summed one row per thread (where those
  * reads would meet shared-memory bank conflicts, each tile arrives by one
  * bulk copy whose barrier wait is bounded: see rdx_wait_timeouts); short and

@@ -4,7 +4,8 @@
 // On the page "03_shared_memory_sync_reduction.py", demo 3, every block writes
 // the sum of its own contiguous segment to out[blockIdx]: a segmented sum.
 // Here a segment is a row, and the work per row decides who sums it:
-//   * narrow rows (contiguous, cols < kNarrowMaxCols; see rowsum_use_narrow):
+//   * narrow rows (contiguous, cols < kNarrowMaxCols, i.e. at most 64; see
+//     rowsum_use_narrow):
 //     the matrix is read as one flat array, tile by tile, into shared
 //     memory, and each thread sums whole rows from there;
 //   * short rows (cols <= kFitRowMaxCols): a group of LPR lanes per row, each
@@ -55,11 +56,13 @@ constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight
 constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
 constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
 constexpr int kNarrowBulkTile = 6144;    // the same with bulk-copy staging (24 KiB: 8 blocks per SM)
-constexpr int64_t kNarrowMaxCols = 64;   // narrow rows: fewer columns than this
+constexpr int64_t kNarrowMaxCols = 65;   // narrow rows: fewer columns than this
 // Rotated reads (see rowsum_narrow_kernel) pay one shared load per VEC-float
-// group of a row; measured against the short-row kernel, they win up to 52
-// groups (1-float reads of 56 columns tie, of 60 columns lose).
-constexpr int kRotatedMaxGroups = 52;
+// group of a row; measured against the short-row kernel at every 4-byte base
+// offset, they win up to a whole 64-column row read one float at a time
+// (64 columns 4-12 bytes off 155.7 -> 148.5-151.6 us per GiB; 56 columns,
+// bulk-staged, 157.7 -> 153.6).
+constexpr int kRotatedMaxGroups = 64;
 
 // Elements of a row before its first 16-byte boundary (rows of a matrix with
 // cols % 4 != 0 start at varying alignments).
@@ -696,12 +699,12 @@ static NarrowRead rowsum_narrow_read(const float* x, int64_t cols, int64_t ld) {
     const int vi = vec == 1 ? 0 : vec == 2 ? 1 : 2;
     // measured: at most 2-way always gains; up to 4-way only for 8 columns or fewer
     const int limit = cols <= 8 ? 4 : 2;
-    // measured over 33-63 columns at every base offset (1 GiB each): the
-    // short-row kernel is faster for rows read one float at a time whose
-    // width is 2 (mod 4) from 50 up (50 columns 4 bytes off 165.9 -> 159.7 us,
-    // 58 columns 163.8 -> 155.7, 62 columns 165.9 -> 153.6), and for 60
-    // columns off 16-byte alignment
-    if (vec == 1 && cols % 4 == 2 && cols >= 50) return NarrowRead::kNo;
+    // measured over 48-64 columns at every base offset (1 GiB each): for
+    // 60 columns off 16-byte alignment the short-row kernel is faster (155.7
+    // against 159.7 us); rows of width 2 (mod 4) from 50 columns up read one
+    // float at a time take the narrow kernel, bulk-staged (50 columns 4 bytes
+    // off 159.7 -> 154.7 us, 54 columns 157.7 -> 153.6, 58 columns 155.7 ->
+    // 153.6, 62 columns a tie)
     if (vec < 4 && cols == 60) return NarrowRead::kNo;
     NarrowRead read = NarrowRead::kNo;
     if (table.ways[cols][vi][0] <= limit) read = NarrowRead::kPlain;

@@ -115,12 +115,13 @@ def test_row_sums_stay_in_bounds(lib, shape):
     assert violations(lib) == 0
 
 
-@pytest.mark.parametrize("cols", [1, 2, 3, 4, 6, 8, 12, 16, 20, 31, 32, 52, 56, 63])
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 6, 8, 12, 16, 20, 31, 32, 40, 50, 52, 56, 63, 64])
 def test_narrow_row_sums_stay_in_bounds(lib, cols):
-    # contiguous rows of fewer than 64 columns: tiles of whole rows staged in
-    # shared memory, at every 4-byte misalignment of the base (the rotated
-    # reads of unaligned 8, 12, 16, ... columns included)
-    rows = 3 * (4096 // cols) + 5
+    # contiguous rows of at most 64 columns: tiles of whole rows staged in
+    # shared memory, at every 4-byte misalignment of the base (the rotated and
+    # aligned-down reads of unaligned 8, 12, 16, ... columns and the bulk-copy
+    # staging included)
+    rows = 3 * (6144 // cols) + 5
     host = inputs.uniform_f32(rows * cols, seed=cols, lo=-1.0, hi=1.0).reshape(rows, cols)
     for offset in range(4):
         x = to_device(host.reshape(-1), offset)

@@ -311,10 +311,11 @@ NARROW_COLS = list(range(1, 66))
 @pytest.mark.parametrize("cols", NARROW_COLS)
 @pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_rowsum_narrow_parity(cols, offset):
-    # rows below 64 columns are staged through shared memory in tiles of
-    # 4096 floats; three whole tiles and a ragged fourth, at every 4-byte
-    # misalignment of the base
-    rows = 3 * (4096 // cols) + 5
+    # rows of at most 64 columns are staged through shared memory in tiles of
+    # 4096 floats (6144 where a bulk copy stages them); three whole tiles and
+    # a ragged fourth of the larger size, at every 4-byte misalignment of the
+    # base
+    rows = 3 * (6144 // cols) + 5
     host = inputs.uniform_f32(rows * cols, seed=cols * 4 + offset, lo=-1.0, hi=1.0).reshape(rows, cols)
     x = to_device(host.reshape(-1), offset).view(rows, cols)
     got = abi.rdx_rowsum_f32(x).cpu().numpy().astype(np.float64)
@@ -324,14 +325,15 @@ def test_rowsum_narrow_parity(cols, offset):
     assert bad.size == 0, (bad[:5], got[bad[:5]], ref[bad[:5]])
 
 
-@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 8, 12, 16, 24, 31, 32, 48, 52, 56, 63])
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 6, 8, 12, 16, 24, 31, 32, 40, 48, 50, 52, 56, 58, 60, 62, 63, 64])
 @pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_rowsum_narrow_exact_integers(cols, offset):
     # small integers: every partial sum is exact in float32, so each row sum
     # must equal the integer sum bit for bit (a misplaced, dropped or doubled
     # element changes it); the unaligned bases of 8, 12, 16, ... columns take
-    # the rotated reads, whose wrap-around this checks element by element
-    rows = 2 * (4096 // cols) + 3
+    # the rotated or aligned-down reads, and of 2, 4, 6, 8, 16, ... columns
+    # the bulk-copy staging, which this checks element by element
+    rows = 2 * (6144 // cols) + 3
     vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
     x = to_device(vals, offset).view(rows, cols)
     got = abi.rdx_rowsum_f32(x).cpu().numpy()

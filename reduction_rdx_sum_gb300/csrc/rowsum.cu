@@ -379,6 +379,68 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     }
 }
 
+// Stage rows [r0, r0 + nr) of the contiguous (rows, cols) matrix x, at most
+// kTile floats, in the block's shared array tile: tile float i (counted from
+// the first float of row r0) lands at tile[s + i], s = (4 - h) mod 4 with h
+// the floats before the first 16-byte boundary, so that the 16-byte body
+// lands on 16-byte boundaries.  BULK: thread 0 starts one bulk copy of the
+// body, tracked by a shared-memory barrier (armed for extra_tx more bytes: 0
+// except in the timeout test, where nothing then completes it); otherwise
+// every thread loads its 16-byte vectors, all in flight together, and stores
+// them.  The up to 3 + 3 floats outside the body are plain loads.  Returns
+// with the tile complete and the block synchronised, or false if the bulk
+// copy's bounded wait gave up: the timeout is counted, the copy is given a
+// second bounded wait to land before the block's shared memory is released,
+// and the block must then write nothing.
+template <int kTile, bool BULK>
+__device__ __forceinline__ bool stage_rows(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t r0,
+                                           int nr, float* tile, int& s, unsigned extra_tx) {
+    const int t = threadIdx.x;
+    const int len = nr * int(cols);                   // floats of this tile, <= kTile
+    const float* __restrict__ p0 = x + r0 * cols;
+    const size_t span = size_t(rows) * size_t(cols) * 4;
+    int h = int(((16u - (unsigned(reinterpret_cast<uintptr_t>(p0)) & 15u)) & 15u) >> 2);
+    if (h > len) h = len;
+    const int m = (len - h) >> 2;                     // whole 16-byte vectors
+    const int tail0 = h + 4 * m;
+    s = -h & 3;
+    const uint4* __restrict__ pv = reinterpret_cast<const uint4*>(p0 + h);
+    if (BULK) {
+        __shared__ __align__(8) unsigned long long bar;
+        __shared__ int staged;
+        if (t == 0) {
+            staged = m > 0 && guard(pv, size_t(m) * 16, x, span);
+            if (staged) bulk_load(tile + s + h, pv, unsigned(m) * 16u, &bar, extra_tx);
+        }
+        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
+        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
+        __syncthreads();  // the barrier is armed, the edge floats are stored
+        if (staged && !mbar_wait_bounded(&bar)) {
+            if (t == 0) atomicAdd(&g_stage_timeouts, 1ull);
+            (void)mbar_wait_bounded(&bar);
+            return false;
+        }
+    } else {
+        constexpr int kLoads = kTile / 4 / kNarrowBlock;  // vectors per thread, all in flight
+        uint4 v[kLoads];
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+            const int k = t + u * kNarrowBlock;
+            v[u] = k < m && guard(pv + k, 16, x, span) ? ld_stream16(pv + k) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        batch_fence(v);
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+            const int k = t + u * kNarrowBlock;
+            if (k < m) *reinterpret_cast<uint4*>(tile + s + h + 4 * k) = v[u];
+        }
+        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
+        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
+        __syncthreads();
+    }
+    return true;
+}
+
 // Narrow rows of a contiguous matrix (ld == cols).  The matrix is read as
 // one flat array cut into tiles of whole rows, at most kNarrowTile floats
 // each, one tile per block.  The block stages its tile in shared memory
@@ -423,55 +485,8 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     const int ci = int(cols);
     const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
     const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
-    const int len = nr * ci;                          // floats of this tile, <= kTile
-    const float* __restrict__ p0 = x + r0 * cols;
-    const size_t span = size_t(rows) * size_t(cols) * 4;
-    int h = int(((16u - (unsigned(reinterpret_cast<uintptr_t>(p0)) & 15u)) & 15u) >> 2);
-    if (h > len) h = len;
-    const int m = (len - h) >> 2;                     // whole 16-byte vectors
-    const int tail0 = h + 4 * m;
-    const int s = -h & 3;                             // tile float i lives at tile[s + i]
-    const uint4* __restrict__ pv = reinterpret_cast<const uint4*>(p0 + h);
-
-    if (BULK) {
-        // one bulk copy of the tile's m vectors, tracked by a shared-memory
-        // barrier (its byte count armed by thread 0 before the copy starts);
-        // extra_tx is 0 except in the timeout test, where it keeps the
-        // barrier from completing
-        __shared__ __align__(8) unsigned long long bar;
-        __shared__ int staged;
-        if (t == 0) {
-            staged = m > 0 && guard(pv, size_t(m) * 16, x, span);
-            if (staged) bulk_load(tile + s + h, pv, unsigned(m) * 16u, &bar, extra_tx);
-        }
-        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
-        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
-        __syncthreads();  // the barrier is armed, the edge floats are stored
-        if (staged && !mbar_wait_bounded(&bar)) {
-            // gave up: count it, let the copy land (a second bounded wait)
-            // before the block's shared memory is released, write nothing
-            if (t == 0) atomicAdd(&g_stage_timeouts, 1ull);
-            (void)mbar_wait_bounded(&bar);
-            return;
-        }
-    } else {
-        constexpr int kLoads = kTile / 4 / kNarrowBlock;  // vectors per thread, all in flight
-        uint4 v[kLoads];
-#pragma unroll
-        for (int u = 0; u < kLoads; ++u) {
-            const int k = t + u * kNarrowBlock;
-            v[u] = k < m && guard(pv + k, 16, x, span) ? ld_stream16(pv + k) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        batch_fence(v);
-#pragma unroll
-        for (int u = 0; u < kLoads; ++u) {
-            const int k = t + u * kNarrowBlock;
-            if (k < m) *reinterpret_cast<uint4*>(tile + s + h + 4 * k) = v[u];
-        }
-        if (t < h && guard(p0 + t, 4, x, span)) tile[s + t] = __ldg(p0 + t);
-        if (t < len - tail0 && guard(p0 + tail0 + t, 4, x, span)) tile[s + tail0 + t] = __ldg(p0 + tail0 + t);
-        __syncthreads();
-    }
+    int s;                                            // tile float i lives at tile[s + i]
+    if (!stage_rows<kTile, BULK>(x, rows, cols, r0, nr, tile, s, extra_tx)) return;
 
     for (int q = t; q < nr; q += kNarrowBlock) {
         const float* row = tile + s + q * ci;
@@ -551,6 +566,49 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     }
 }
 
+// Short rows that the short-row kernel would leave with half-empty load
+// slots (see rowsum_staged_lanes): tiles of whole rows staged as in the
+// narrow kernel, by one bulk copy each (24 KiB, 8 blocks per SM, so the
+// bytes in flight do not depend on the width), then summed from shared
+// memory by groups of LW lanes: lane l of a group adds words l, l + LW, ...
+// of its row in two alternating chains, the group's shuffle tree adds the
+// lanes, and its first lane stores the sum.  The lanes of a warp read
+// consecutive words of a row, so the reads meet no bank conflict whatever
+// the row's alignment.  The order depends on cols and LW only.
+template <int LW>
+__global__ void __launch_bounds__(kNarrowBlock)
+rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
+                     float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
+    __shared__ __align__(16) float tile[kNarrowBulkTile + 4];
+    const int ci = int(cols);
+    const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
+    const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
+    int s;
+    if (!stage_rows<kNarrowBulkTile, true>(x, rows, cols, r0, nr, tile, s, 0u)) return;
+    constexpr int kGroups = kWarpSize / LW;           // rows per warp step
+    const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+    const int g = lane / LW, l = lane % LW;
+    // the loop bound is the same for every lane of a warp, so the shuffle
+    // tree always has the whole warp
+    for (int qb = warp * kGroups; qb < nr; qb += (kNarrowBlock / kWarpSize) * kGroups) {
+        const int q = qb + g;
+        float a0 = 0.f, a1 = 0.f;
+        if (q < nr) {
+            const float* row = tile + s + q * ci;
+            int j = l;
+            for (; j + LW < ci; j += 2 * LW) {
+                a0 += row[j];
+                a1 += row[j + LW];
+            }
+            if (j < ci) a0 += row[j];
+        }
+        const float v = group_allreduce<LW>(a0 + a1);
+        if (l == 0 && q < nr && guard(out + r0 + q, 4, out, size_t(rows) * 4)) out[r0 + q] = v;
+    }
+}
+
 // Lanes per row: the fewest (a power of two, at most 32) that leave each lane
 // at most four 16-byte vectors of the row.
 int lanes_per_row(int64_t cols) {
@@ -558,6 +616,44 @@ int lanes_per_row(int64_t cols) {
     int lpr = 1;
     while (lpr < 32 && int64_t(lpr) * 4 < vecs) lpr *= 2;
     return lpr;
+}
+
+// Lanes per row of the staged kernel for the contiguous (rows, cols) matrix
+// at x, or 0 where the short-row kernel keeps the rows.  That kernel gives a
+// row the fewest lanes, a power of two, that leave each lane at most four
+// 16-byte vectors, so a row just past a power of two fills about half of
+// its lanes' load slots (68 columns: 17 vectors in 8 lanes x 4), keeps half
+// the bytes in flight and reads well below the bandwidth (measured, 1 GiB:
+// 68 columns 4 bytes off 202.8 us, 132 columns 210.9, 260 columns 200.7,
+// against 145-150 us for rows that fill their slots).  The staged kernel
+// holds 147-155 us at the widths it takes, so it takes the rows whose slots
+// the short-row kernel would fill less than 60 % (16-byte aligned rows,
+// which that kernel reads faster at equal fill) or 75 % (rows not all
+// aligned; 80 % from 257 columns, where the staged kernel's groups of 32
+// lanes still win at 78-80 %); measured over 65-512 columns at 0 and 4
+// bytes off.  Groups of 8 lanes below 96 columns, 16 below 256, 32 above
+// (the fastest in the same sweep); a warp's groups of 8 read 4 rows at once,
+// cols words apart, and where they would share a bank more than 2 ways
+// (93-95 columns) the short-row kernel keeps the rows.
+static int staged_group_bank_ways(int64_t cols, int lw) {
+    int count[kWarpSize] = {};
+    for (int g = 0; g < kWarpSize / lw; ++g)
+        for (int l = 0; l < lw; ++l) ++count[(g * cols + l) % kWarpSize];
+    int worst = 0;
+    for (int b = 0; b < kWarpSize; ++b) worst = worst > count[b] ? worst : count[b];
+    return worst;
+}
+
+static int rowsum_staged_lanes(const float* x, int64_t cols, int64_t ld) {
+    if (ld != cols || cols < kNarrowMaxCols || cols > kFitRowMaxCols) return 0;
+    const int lpr = lanes_per_row(cols);
+    const int64_t vecs = cols / 4, slots = 4 * int64_t(lpr);
+    const bool aligned = cols % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
+    const bool sparse = aligned ? 10 * vecs < 6 * slots : lpr == 32 ? 10 * vecs < 8 * slots : 4 * vecs < 3 * slots;
+    if (!sparse) return 0;
+    const int lw = cols < 96 ? 8 : cols < 256 ? 16 : 32;
+    if (lw == 8 && staged_group_bank_ways(cols, 8) > 2) return 0;
+    return lw;
 }
 
 template <int LPR>
@@ -789,6 +885,15 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
                            : launch_pdl(rowsum_narrow_kernel<1, false, false, false>, grid, block, stream, x, rows, cols,
                                         rpt, out, 0u);
         }
+    }
+    if (const int lw = rowsum_staged_lanes(x, cols, ld)) {
+        const int64_t rpt = kNarrowBulkTile / cols;  // whole rows per tile
+        const int64_t blocks = (rows + rpt - 1) / rpt;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
+        if (lw == 8) return launch_pdl(rowsum_staged_kernel<8>, grid, block, stream, x, rows, cols, rpt, out);
+        if (lw == 16) return launch_pdl(rowsum_staged_kernel<16>, grid, block, stream, x, rows, cols, rpt, out);
+        return launch_pdl(rowsum_staged_kernel<32>, grid, block, stream, x, rows, cols, rpt, out);
     }
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {

@@ -133,6 +133,22 @@ def test_narrow_row_sums_stay_in_bounds(lib, cols):
     assert violations(lib) == 0
 
 
+@pytest.mark.parametrize("cols", [68, 92, 132, 184, 260, 400])
+def test_staged_row_sums_stay_in_bounds(lib, cols):
+    # contiguous rows of 65-512 columns staged in 24 KiB tiles by one bulk
+    # copy each, at every 4-byte misalignment of the base
+    rows = 3 * (6144 // cols) + 5
+    host = inputs.uniform_f32(rows * cols, seed=cols, lo=-1.0, hi=1.0).reshape(rows, cols)
+    for offset in range(4):
+        x = to_device(host.reshape(-1), offset)
+        out = torch.empty(rows, device=DEV)
+        assert lib.rdx_rowsum_strided_f32(x.data_ptr(), rows, cols, cols, out.data_ptr(), stream()) == 0
+        torch.cuda.synchronize()
+        tol = 1e-6 * oracle.rowabssum_f32(host) + 1e-30
+        assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - oracle.rowsum_f32(host)) <= tol)
+    assert violations(lib) == 0
+
+
 def test_ladder_stays_in_bounds(lib):
     for v in range(1, 6):
         for n in (1, 255, 257, 513, (1 << 16) + 77):

@@ -342,6 +342,29 @@ def test_rowsum_narrow_exact_integers(cols, offset):
     assert np.array_equal(oracle.rowsum_f32(vals.reshape(rows, cols)), want.astype(np.float64))
 
 
+STAGED_COLS = [68, 70, 72, 76, 80, 92, 93, 94, 96, 100, 132, 140, 148, 184, 191, 192, 196, 260, 264, 300, 350, 380, 400, 409, 410]
+
+
+@pytest.mark.parametrize("cols", STAGED_COLS)
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_rowsum_staged_exact_integers(cols, offset):
+    # rows of 65-512 columns whose lanes the short-row kernel would leave
+    # half-empty go through shared memory in 24 KiB tiles (one bulk copy
+    # each) and are summed by groups of 8, 16 or 32 lanes: three whole tiles
+    # and a ragged fourth, small integers so every row sum is exact, at every
+    # 4-byte misalignment of the base; the widths on either side of each rule
+    # boundary stay with the short-row kernel and must agree too
+    rows = 3 * (6144 // cols) + 5
+    vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
+    x = to_device(vals, offset).view(rows, cols)
+    got = abi.rdx_rowsum_f32(x).cpu().numpy()
+    want = vals.reshape(rows, cols).astype(np.int64).sum(axis=1)
+    assert np.array_equal(got.astype(np.int64), want)
+    host = inputs.uniform_f32(rows * cols, seed=cols + offset, lo=-1.0, hi=1.0).reshape(rows, cols)
+    got = abi.rdx_rowsum_f32(to_device(host.reshape(-1), offset).view(rows, cols)).cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - oracle.rowsum_f32(host)) <= 1e-6 * oracle.rowabssum_f32(host) + 1e-30)
+
+
 @pytest.mark.parametrize("shape", [(100, 257), (64, 1001), (20, 2049), (12, 4095), (40, 5121), (300, 6001),
                                    (2100, 16385)], ids=str)
 @pytest.mark.parametrize("offset", [0, 1, 2, 3])

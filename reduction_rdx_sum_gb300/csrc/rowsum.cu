@@ -56,6 +56,8 @@ constexpr int kRowSteps = RDX_ROW_STEPS;  // row steps whose loads are in flight
 constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
 constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
 constexpr int kNarrowBulkTile = 6144;    // the same with bulk-copy staging (24 KiB: 8 blocks per SM)
+constexpr int64_t kStagedMaxCols = 6000;  // widest rows the staged kernel takes (a tile holds one row at least)
+static_assert(kStagedMaxCols <= kNarrowBulkTile, "a staged tile must hold a whole row");
 constexpr int64_t kNarrowMaxCols = 65;   // narrow rows: fewer columns than this
 // Rotated reads (see rowsum_narrow_kernel) pay one shared load per VEC-float
 // group of a row; measured against the short-row kernel at every 4-byte base
@@ -634,7 +636,14 @@ int lanes_per_row(int64_t cols) {
 // bytes off.  Groups of 8 lanes below 96 columns, 16 below 256, 32 above
 // (the fastest in the same sweep); a warp's groups of 8 read 4 rows at once,
 // cols words apart, and where they would share a bank more than 2 ways
-// (93-95 columns) the short-row kernel keeps the rows.
+// (93-95 columns) the short-row kernel keeps the rows.  Contiguous rows of
+// 513 to kStagedMaxCols columns take it with groups of 32 lanes at every
+// width and alignment: measured faster or equal against the warp-per-row
+// and block-per-row kernels over 513-6144 columns at 0, 4 and 8 bytes off
+// (1 GiB: 516 columns 4-8 bytes off 159.8-161.8 -> 149.5 us, 600 columns
+// 157.7 -> 149.5, 1500 columns 155.7 -> 147.5, 5200 columns 156.7 -> 147.5;
+// 1024 columns aligned and 6144 columns 4 bytes off one timer tick slower,
+// 6000 columns equal).
 static int staged_group_bank_ways(int64_t cols, int lw) {
     int count[kWarpSize] = {};
     for (int g = 0; g < kWarpSize / lw; ++g)
@@ -645,7 +654,8 @@ static int staged_group_bank_ways(int64_t cols, int lw) {
 }
 
 static int rowsum_staged_lanes(const float* x, int64_t cols, int64_t ld) {
-    if (ld != cols || cols < kNarrowMaxCols || cols > kFitRowMaxCols) return 0;
+    if (ld != cols || cols < kNarrowMaxCols || cols > kStagedMaxCols) return 0;
+    if (cols > kFitRowMaxCols) return 32;
     const int lpr = lanes_per_row(cols);
     const int64_t vecs = cols / 4, slots = 4 * int64_t(lpr);
     const bool aligned = cols % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;

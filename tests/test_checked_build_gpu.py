@@ -133,7 +133,7 @@ def test_narrow_row_sums_stay_in_bounds(lib, cols):
     assert violations(lib) == 0
 
 
-@pytest.mark.parametrize("cols", [68, 92, 132, 184, 260, 400])
+@pytest.mark.parametrize("cols", [68, 92, 132, 184, 260, 400, 600, 3073, 6000])
 def test_staged_row_sums_stay_in_bounds(lib, cols):
     # contiguous rows of 65-512 columns staged in 24 KiB tiles by one bulk
     # copy each, at every 4-byte misalignment of the base

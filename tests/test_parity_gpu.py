@@ -342,18 +342,20 @@ def test_rowsum_narrow_exact_integers(cols, offset):
     assert np.array_equal(oracle.rowsum_f32(vals.reshape(rows, cols)), want.astype(np.float64))
 
 
-STAGED_COLS = [68, 70, 72, 76, 80, 92, 93, 94, 96, 100, 132, 140, 148, 184, 191, 192, 196, 260, 264, 300, 350, 380, 400, 409, 410]
+STAGED_COLS = [68, 70, 72, 76, 80, 92, 93, 94, 96, 100, 132, 140, 148, 184, 191, 192, 196, 260, 264, 300, 350, 380,
+               400, 409, 410, 512, 513, 600, 1024, 2049, 3072, 3073, 5200, 6000, 6001]
 
 
 @pytest.mark.parametrize("cols", STAGED_COLS)
 @pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_rowsum_staged_exact_integers(cols, offset):
     # rows of 65-512 columns whose lanes the short-row kernel would leave
-    # half-empty go through shared memory in 24 KiB tiles (one bulk copy
-    # each) and are summed by groups of 8, 16 or 32 lanes: three whole tiles
-    # and a ragged fourth, small integers so every row sum is exact, at every
-    # 4-byte misalignment of the base; the widths on either side of each rule
-    # boundary stay with the short-row kernel and must agree too
+    # half-empty, and every row of 513-6000 columns, go through shared memory
+    # in 24 KiB tiles (one bulk copy each) and are summed by groups of 8, 16
+    # or 32 lanes: three whole tiles and a ragged fourth, small integers so
+    # every row sum is exact, at every 4-byte misalignment of the base; the
+    # widths on either side of each rule boundary take other kernels and must
+    # agree too
     rows = 3 * (6144 // cols) + 5
     vals = (np.arange(rows * cols) * 7919 % 23).astype(np.float32) - 11
     x = to_device(vals, offset).view(rows, cols)
@@ -377,6 +379,23 @@ def test_rowsum_wide_exact_integers(shape, offset):
     x = to_device(vals, offset).view(rows, cols)
     got = abi.rdx_rowsum_f32(x).cpu().numpy()
     want = vals.reshape(rows, cols).astype(np.int64).sum(axis=1)
+    assert np.array_equal(got.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("shape", [(100, 257), (64, 1001), (20, 2049), (12, 4095), (40, 5121), (300, 6001)],
+                         ids=str)
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_rowsum_strided_exact_integers(shape, offset):
+    # the same rows read through a leading dimension of cols + 3 (every row at
+    # its own alignment): contiguous rows of these widths take the staged
+    # kernel, these the short-row, warp-per-row (its edge-float variant from
+    # 2048 columns) and block-per-row kernels
+    rows, cols = shape
+    ld = cols + 3
+    vals = (np.arange(rows * ld) * 7919 % 23).astype(np.float32) - 11
+    x = to_device(vals, offset).view(rows, ld)[:, :cols]
+    got = abi.rdx_rowsum_strided_f32(x).cpu().numpy()
+    want = vals.reshape(rows, ld)[:, :cols].astype(np.int64).sum(axis=1)
     assert np.array_equal(got.astype(np.int64), want)
 
 

@@ -198,9 +198,9 @@ rdx_status rdx_max_i32(const int32_t* x, int64_t n, int32_t* out, cudaStream_t s
  * memory in tiles of whole rows and summed one row per thread (where those
  * reads would meet shared-memory bank conflicts, each tile arrives by one
  * bulk copy whose barrier wait is bounded: see rdx_wait_timeouts); short and
- * medium rows are summed by a group of threads each (contiguous rows of up
- * to 6000 columns that those groups would read with half-empty load slots,
- * and every row of 513 to 6000 columns, from tiles staged the same way),
+ * medium rows are summed by a group of threads each (from tiles staged the
+ * same way: contiguous rows of 65 to 512 columns that a group would read
+ * with half-empty load slots, and every contiguous row of 513 to 6000),
  * long rows by a block each, with no workspace.  Few, very long rows (fewer than two waves of
  * blocks, at least 16384 columns, at most 2048 rows) are each cut into tiles
  * over many blocks and finished on the device like the scalar sums; that

@@ -57,6 +57,8 @@ constexpr int kNarrowBlock = 256;        // threads per block, narrow rows
 constexpr int kNarrowTile = 4096;        // floats staged per block (16 KiB), narrow rows
 constexpr int kNarrowBulkTile = 6144;    // the same with bulk-copy staging (24 KiB: 8 blocks per SM)
 constexpr int64_t kStagedMaxCols = 6000;  // widest rows the staged kernel takes (a tile holds one row at least)
+constexpr int64_t kStagedMaxGap = 8;      // rows with a leading dimension: staged as one span below this gap
+constexpr int64_t kRowsStagedMinCols = 1500;  // wider gaps: one bulk copy per row from this width
 static_assert(kStagedMaxCols <= kNarrowBulkTile, "a staged tile must hold a whole row");
 constexpr int64_t kNarrowMaxCols = 65;   // narrow rows: fewer columns than this
 // Rotated reads (see rowsum_narrow_kernel) pay one shared load per VEC-float
@@ -97,6 +99,26 @@ __device__ __forceinline__ void bulk_load(float* dst, const void* src, unsigned 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes + extra)
                  : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// The same barrier driven by several threads: thread 0 initialises it for
+// one arrival, every thread that starts a copy first adds its bytes to the
+// barrier's expected count (mbar_expect_bytes), and thread 0 arrives only
+// after a block-wide barrier has ordered every addition before it, so the
+// phase cannot complete before the last copy's bytes have landed.
+__device__ __forceinline__ void mbar_init_one(unsigned long long* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_bytes(unsigned long long* bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_copy(float* dst, const void* src, unsigned bytes, unsigned long long* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
@@ -381,9 +403,11 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
     }
 }
 
-// Stage rows [r0, r0 + nr) of the contiguous (rows, cols) matrix x, at most
-// kTile floats, in the block's shared array tile: tile float i (counted from
-// the first float of row r0) lands at tile[s + i], s = (4 - h) mod 4 with h
+// Stage rows [r0, r0 + nr) of the (rows, cols) matrix x whose rows start
+// every ld floats, as the one span from the first float of row r0 to the
+// last of row r0 + nr - 1 (at most kTile floats; the gaps between rows come
+// along), in the block's shared array tile: span float i lands at
+// tile[s + i], s = (4 - h) mod 4 with h
 // the floats before the first 16-byte boundary, so that the 16-byte body
 // lands on 16-byte boundaries.  BULK: thread 0 starts one bulk copy of the
 // body, tracked by a shared-memory barrier (armed for extra_tx more bytes: 0
@@ -395,12 +419,12 @@ rowsum_cta_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64
 // second bounded wait to land before the block's shared memory is released,
 // and the block must then write nothing.
 template <int kTile, bool BULK>
-__device__ __forceinline__ bool stage_rows(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t r0,
-                                           int nr, float* tile, int& s, unsigned extra_tx) {
+__device__ __forceinline__ bool stage_rows(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                                           int64_t r0, int nr, float* tile, int& s, unsigned extra_tx) {
     const int t = threadIdx.x;
-    const int len = nr * int(cols);                   // floats of this tile, <= kTile
-    const float* __restrict__ p0 = x + r0 * cols;
-    const size_t span = size_t(rows) * size_t(cols) * 4;
+    const int len = (nr - 1) * int(ld) + int(cols);  // floats of this tile's span, <= kTile
+    const float* __restrict__ p0 = x + r0 * ld;
+    const size_t span = (size_t(rows - 1) * size_t(ld) + size_t(cols)) * 4;
     int h = int(((16u - (unsigned(reinterpret_cast<uintptr_t>(p0)) & 15u)) & 15u) >> 2);
     if (h > len) h = len;
     const int m = (len - h) >> 2;                     // whole 16-byte vectors
@@ -488,7 +512,7 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
     const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
     int s;                                            // tile float i lives at tile[s + i]
-    if (!stage_rows<kTile, BULK>(x, rows, cols, r0, nr, tile, s, extra_tx)) return;
+    if (!stage_rows<kTile, BULK>(x, rows, cols, cols, r0, nr, tile, s, extra_tx)) return;
 
     for (int q = t; q < nr; q += kNarrowBlock) {
         const float* row = tile + s + q * ci;
@@ -579,7 +603,7 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
 // the row's alignment.  The order depends on cols and LW only.
 template <int LW>
 __global__ void __launch_bounds__(kNarrowBlock)
-rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t rows_per_tile,
+rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t rows_per_tile,
                      float* __restrict__ out) {
     pdl_wait();     // the previous kernel in the stream has finished writing
     pdl_release();  // the next one may be scheduled into SMs this grid frees
@@ -588,7 +612,7 @@ rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
     const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
     int s;
-    if (!stage_rows<kNarrowBulkTile, true>(x, rows, cols, r0, nr, tile, s, 0u)) return;
+    if (!stage_rows<kNarrowBulkTile, true>(x, rows, cols, ld, r0, nr, tile, s, 0u)) return;
     constexpr int kGroups = kWarpSize / LW;           // rows per warp step
     const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
     const int g = lane / LW, l = lane % LW;
@@ -598,7 +622,74 @@ rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
         const int q = qb + g;
         float a0 = 0.f, a1 = 0.f;
         if (q < nr) {
-            const float* row = tile + s + q * ci;
+            const float* row = tile + s + q * int(ld);
+            int j = l;
+            for (; j + LW < ci; j += 2 * LW) {
+                a0 += row[j];
+                a1 += row[j + LW];
+            }
+            if (j < ci) a0 += row[j];
+        }
+        const float v = group_allreduce<LW>(a0 + a1);
+        if (l == 0 && q < nr && guard(out + r0 + q, 4, out, size_t(rows) * 4)) out[r0 + q] = v;
+    }
+}
+
+// Short and medium rows with a leading dimension (ld > cols), where every
+// row has its own alignment: the rows of a tile are staged one bulk copy per
+// row, each row's 16-byte body into a slot of W words (a multiple of 4 with
+// 4 spare words in front), its up to 3 + 3 edge floats by plain loads, so
+// that row q's words occupy [q W + 4 - h, q W + 4 - h + cols) with h the
+// row's floats before its first 16-byte boundary.  W is padded so that the
+// kGroups rows a warp reads at once start LW words apart modulo 32: the
+// groups read disjoint banks.  Rows are then summed as in
+// rowsum_staged_kernel (groups of LW lanes, two alternating chains per lane,
+// the group's shuffle tree), so a row's sum has the same bits either way.
+template <int LW>
+__global__ void __launch_bounds__(kNarrowBlock)
+rowsum_rows_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t slot,
+                          int64_t rows_per_tile, float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
+    __shared__ __align__(16) float tile[kNarrowBulkTile];
+    __shared__ __align__(8) unsigned long long bar;
+    const int t = threadIdx.x;
+    const int ci = int(cols), w = int(slot);
+    const int64_t r0 = int64_t(blockIdx.x) * rows_per_tile;
+    const int nr = int(rows - r0 < rows_per_tile ? rows - r0 : rows_per_tile);
+    const size_t span = (size_t(rows - 1) * size_t(ld) + size_t(cols)) * 4;
+    if (t == 0) mbar_init_one(&bar);
+    __syncthreads();  // the barrier is initialised
+    for (int q = t; q < nr; q += kNarrowBlock) {
+        const float* __restrict__ row = x + (r0 + q) * ld;
+        const int h = int(row_head(row, cols));
+        const int m = (ci - h) >> 2;
+        const int tail0 = h + 4 * m;
+        float* dst = tile + q * w + 4;
+        if (m > 0 && guard(row + h, size_t(m) * 16, x, span)) {
+            mbar_expect_bytes(&bar, unsigned(m) * 16u);
+            bulk_copy(dst, row + h, unsigned(m) * 16u, &bar);
+        }
+        for (int e = 0; e < h; ++e)
+            if (guard(row + e, 4, x, span)) dst[e - h] = __ldg(row + e);
+        for (int e = tail0; e < ci; ++e)
+            if (guard(row + e, 4, x, span)) dst[e - h] = __ldg(row + e);
+    }
+    __syncthreads();  // every expected byte count is in, the edge floats are stored
+    if (t == 0) mbar_arrive(&bar);
+    if (!mbar_wait_bounded(&bar)) {
+        if (t == 0) atomicAdd(&g_stage_timeouts, 1ull);
+        (void)mbar_wait_bounded(&bar);
+        return;
+    }
+    constexpr int kGroups = kWarpSize / LW;
+    const int warp = t / kWarpSize, lane = t % kWarpSize;
+    const int g = lane / LW, l = lane % LW;
+    for (int qb = warp * kGroups; qb < nr; qb += (kNarrowBlock / kWarpSize) * kGroups) {
+        const int q = qb + g;
+        float a0 = 0.f, a1 = 0.f;
+        if (q < nr) {
+            const float* row = tile + q * w + 4 - int(row_head(x + (r0 + q) * ld, cols));
             int j = l;
             for (; j + LW < ci; j += 2 * LW) {
                 a0 += row[j];
@@ -654,16 +745,36 @@ static int staged_group_bank_ways(int64_t cols, int lw) {
 }
 
 static int rowsum_staged_lanes(const float* x, int64_t cols, int64_t ld) {
-    if (ld != cols || cols < kNarrowMaxCols || cols > kStagedMaxCols) return 0;
+    if (ld - cols >= kStagedMaxGap || cols < kNarrowMaxCols || cols > kStagedMaxCols) return 0;
     if (cols > kFitRowMaxCols) return 32;
     const int lpr = lanes_per_row(cols);
     const int64_t vecs = cols / 4, slots = 4 * int64_t(lpr);
-    const bool aligned = cols % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
+    const bool aligned = cols % 4 == 0 && ld % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
     const bool sparse = aligned ? 10 * vecs < 6 * slots : lpr == 32 ? 10 * vecs < 8 * slots : 4 * vecs < 3 * slots;
     if (!sparse) return 0;
     const int lw = cols < 96 ? 8 : cols < 256 ? 16 : 32;
-    if (lw == 8 && staged_group_bank_ways(cols, 8) > 2) return 0;
+    if (lw == 8 && staged_group_bank_ways(ld, 8) > 2) return 0;
     return lw;
+}
+
+// Row slot of rowsum_rows_staged_kernel for rows of cols floats read by
+// groups of lw lanes: at least cols + 4 words, a multiple of 4, and for
+// groups of 8 or 16 an odd multiple of lw modulo 32, so that the 32 / lw
+// rows a warp reads at once start in different banks.
+static int64_t rows_staged_slot(int64_t cols, int lw) {
+    int64_t w = (cols + 4 + 3) / 4 * 4;
+    if (lw < kWarpSize)
+        while ((w / lw) % 2 == 0 || w % lw != 0) w += 4;
+    return w;
+}
+
+// Lanes per row of rowsum_rows_staged_kernel for rows with a leading
+// dimension (ld > cols), or 0 where the short-row, warp-per-row and
+// block-per-row kernels keep them: the same rule as for contiguous rows
+// (rows_staged has the same half-empty short-row slots to avoid), with
+// "aligned" meaning every row 16-byte aligned.
+static int rowsum_rows_staged_lanes(const float*, int64_t cols, int64_t ld) {
+    return ld - cols >= kStagedMaxGap && cols >= kRowsStagedMinCols && cols <= kStagedMaxCols ? 32 : 0;
 }
 
 template <int LPR>
@@ -896,14 +1007,26 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
                                         rpt, out, 0u);
         }
     }
-    if (const int lw = rowsum_staged_lanes(x, cols, ld)) {
-        const int64_t rpt = kNarrowBulkTile / cols;  // whole rows per tile
+    if (const int lw = rowsum_rows_staged_lanes(x, cols, ld)) {
+        const int64_t w = rows_staged_slot(cols, lw);
+        const int64_t rpt = kNarrowBulkTile / w;  // whole rows per tile
         const int64_t blocks = (rows + rpt - 1) / rpt;
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
         const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
-        if (lw == 8) return launch_pdl(rowsum_staged_kernel<8>, grid, block, stream, x, rows, cols, rpt, out);
-        if (lw == 16) return launch_pdl(rowsum_staged_kernel<16>, grid, block, stream, x, rows, cols, rpt, out);
-        return launch_pdl(rowsum_staged_kernel<32>, grid, block, stream, x, rows, cols, rpt, out);
+        if (lw == 8)
+            return launch_pdl(rowsum_rows_staged_kernel<8>, grid, block, stream, x, rows, cols, ld, w, rpt, out);
+        if (lw == 16)
+            return launch_pdl(rowsum_rows_staged_kernel<16>, grid, block, stream, x, rows, cols, ld, w, rpt, out);
+        return launch_pdl(rowsum_rows_staged_kernel<32>, grid, block, stream, x, rows, cols, ld, w, rpt, out);
+    }
+    if (const int lw = rowsum_staged_lanes(x, cols, ld)) {
+        const int64_t rpt = (kNarrowBulkTile - cols) / ld + 1;  // whole rows per tile (their span fits)
+        const int64_t blocks = (rows + rpt - 1) / rpt;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        const dim3 grid{unsigned(blocks)}, block{unsigned(kNarrowBlock)};
+        if (lw == 8) return launch_pdl(rowsum_staged_kernel<8>, grid, block, stream, x, rows, cols, ld, rpt, out);
+        if (lw == 16) return launch_pdl(rowsum_staged_kernel<16>, grid, block, stream, x, rows, cols, ld, rpt, out);
+        return launch_pdl(rowsum_staged_kernel<32>, grid, block, stream, x, rows, cols, ld, rpt, out);
     }
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {

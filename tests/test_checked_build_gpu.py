@@ -149,6 +149,28 @@ def test_staged_row_sums_stay_in_bounds(lib, cols):
     assert violations(lib) == 0
 
 
+@pytest.mark.parametrize("cols", [68, 132, 260, 600, 6000])
+def test_rows_staged_stay_in_bounds(lib, cols):
+    # rows with a leading dimension, each row bulk-copied into its own slot,
+    # at every 4-byte misalignment of the base; the last row ends at the
+    # buffer's end
+    ld = cols + 3
+    rows = 3 * max(1, 6144 // (cols + 32)) + 5
+    n = (rows - 1) * ld + cols
+    host = inputs.uniform_f32(n, seed=cols, lo=-1.0, hi=1.0)
+    full = np.zeros(rows * ld, np.float32)
+    full[:n] = host
+    ref_rows = full.reshape(rows, ld)[:, :cols]
+    for offset in range(4):
+        x = to_device(host, offset)
+        out = torch.empty(rows, device=DEV)
+        assert lib.rdx_rowsum_strided_f32(x.data_ptr(), rows, cols, ld, out.data_ptr(), stream()) == 0
+        torch.cuda.synchronize()
+        tol = 1e-6 * oracle.rowabssum_f32(np.ascontiguousarray(ref_rows)) + 1e-30
+        assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - oracle.rowsum_f32(np.ascontiguousarray(ref_rows))) <= tol)
+    assert violations(lib) == 0
+
+
 def test_ladder_stays_in_bounds(lib):
     for v in range(1, 6):
         for n in (1, 255, 257, 513, (1 << 16) + 77):

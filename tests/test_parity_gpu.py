@@ -399,6 +399,44 @@ def test_rowsum_strided_exact_integers(shape, offset):
     assert np.array_equal(got.astype(np.int64), want)
 
 
+ROWS_STAGED_COLS = [65, 68, 92, 93, 132, 191, 192, 260, 409, 513, 2049, 6000, 6001]
+
+
+@pytest.mark.parametrize("cols", ROWS_STAGED_COLS)
+@pytest.mark.parametrize("pad", [1, 3, 4, 8])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_rowsum_rows_staged_exact_integers(cols, pad, offset):
+    # rows with a leading dimension of cols + pad: where the short-row or
+    # warp-per-row kernel would leave load slots empty, each row's 16-byte
+    # body is bulk-copied into its own padded slot of shared memory and its
+    # edge floats loaded one by one; three whole tiles and a ragged fourth,
+    # small integers so every row sum is exact
+    ld = cols + pad
+    slot = (cols + 4 + 3) // 4 * 4
+    rows = 3 * max(1, 6144 // (slot + 28)) + 5
+    vals = (np.arange(rows * ld) * 7919 % 23).astype(np.float32) - 11
+    x = to_device(vals, offset).view(rows, ld)[:, :cols]
+    got = abi.rdx_rowsum_strided_f32(x).cpu().numpy()
+    want = vals.reshape(rows, ld)[:, :cols].astype(np.int64).sum(axis=1)
+    assert np.array_equal(got.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("cols", [69, 133, 261, 777])
+def test_rows_staged_matches_contiguous_bits(cols):
+    # odd widths: the same rows summed contiguously (one bulk copy per tile)
+    # and through a leading dimension (one bulk copy per row) take the same
+    # lanes and the same order, so their sums agree bit for bit
+    rows = 5000
+    host = inputs.uniform_f32(rows * cols, seed=cols, lo=-1.0, hi=1.0).reshape(rows, cols)
+    contiguous = abi.rdx_rowsum_f32(to_device(host.reshape(-1), 1).view(rows, cols))
+    wide = np.zeros((rows, cols + 5), np.float32)
+    wide[:, :cols] = host
+    strided = abi.rdx_rowsum_strided_f32(to_device(wide.reshape(-1), 2).view(rows, cols + 5)[:, :cols])
+    assert torch.equal(contiguous.view(torch.int32), strided.view(torch.int32))
+    ref = oracle.rowsum_f32(host)
+    assert np.all(np.abs(strided.cpu().numpy().astype(np.float64) - ref) <= 1e-6 * oracle.rowabssum_f32(host) + 1e-30)
+
+
 def test_rowsum_narrow_deterministic_and_matches_strided():
     for cols in (3, 6, 12, 20, 45):
         x = torch.rand((20_000, cols), device=DEV) * 2 - 1

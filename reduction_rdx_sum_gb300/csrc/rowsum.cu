@@ -12,17 +12,24 @@
 //     lane holding at most four 16-byte vectors of the row, so a warp sums
 //     32/LPR consecutive rows per step; the loads of kRowSteps steps are
 //     issued together before any of them is reduced;
-//   * medium rows (cols <= kGroupRowMaxCols): a warp per row, looping over
-//     the row four vectors per lane at a time;
+//   * staged rows (see rowsum_staged_lanes): short rows that would leave
+//     those lanes' load slots half empty, and medium rows up to
+//     kStagedMaxCols, are staged like narrow rows, 24 KiB of whole rows per
+//     bulk copy, and summed from shared memory by a group of lanes per row;
+//     rows with a leading dimension join them when the gap between rows is
+//     small (the span is copied, gaps included), or from kRowsStagedMinCols
+//     columns one bulk copy per row;
+//   * other medium rows (cols <= kGroupRowMaxCols): a warp per row, looping
+//     over the row four vectors per lane at a time;
 //   * long rows: one block per row, the same add-on-load loop and block tree
 //     as the scalar reduction (twice the loads in flight at half the
 //     occupancy from kCtaDeepCols columns), a direct store of the row's sum.
 // Rows may start every ld >= cols elements (a leading dimension).  Rows that
 // are not 16-byte aligned have up to 3 floats before their first and after
 // their last whole vector: the narrow kernel reads such rows from shared
-// memory in a rotated order, the others fetch those edge floats without
-// holding the row's vector loads back (cp.async copies, or registers loaded
-// ahead).  Every kernel is launched with programmatic dependent launch.  A
+// memory in a rotated order, the staged kernels load them one by one beside
+// the bulk copy, and the others fetch them without holding the row's vector
+// loads back (cp.async copies, or registers loaded ahead).  Every kernel is launched with programmatic dependent launch.  A
 // row's summation order depends only on the shape and the alignment of x,
 // never on the grid or the device, so the result is bitwise reproducible.  No
 // workspace is needed.  (Few, very long rows go to the tiled kernel of
@@ -38,12 +45,6 @@ constexpr int kCtaUnroll = 4;    // 16-byte loads in flight per thread, long row
 constexpr int kCtaUnrollDeep = 8;   // the same for rows of kCtaDeepCols or more, at 4 blocks per SM
 constexpr int64_t kCtaDeepCols = 16384;  // measured: deeper is 1 % faster from here, slower below
 constexpr int kGroupBlock = 256; // threads per block, short rows
-// The warp-per-row kernel's variant for rows that are not 16-byte aligned
-// (edge floats copied with cp.async) needs 43 registers against 32: it wins
-// from about 2048 columns (1 GiB of 4095 columns 153.6 -> 151.6 us, 4096
-// columns 12 bytes off 155.6 -> 151.6 us) and loses below (513 columns
-// 157.7 -> 197 us, 1001 columns 151.6 -> 170 us).
-constexpr int64_t kGroupEdgeMinCols = 2048;
 #ifndef RDX_GROUP_ROW_MAX_COLS
 #define RDX_GROUP_ROW_MAX_COLS 5120
 #endif
@@ -148,59 +149,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar) {
     }
 }
 
-// Sum of lane l's share of one row, the row split among LPR lanes.  With
-// EDGES (the matrix has rows that are not 16-byte aligned) the up to 3 + 3
-// floats before the first and after the last whole vector are copied with
-// cp.async to the thread's slots edge[0], edge[stride], ... ahead of the
-// vector loads and added to acc[0] and acc[1] just before the first vector
-// is: the same additions in the same order as adding them on arrival
-// (without EDGES), without holding the warp for their round trip first.
-template <int LPR, bool EDGES>
-__device__ __forceinline__ float row_share(const float* __restrict__ row, int64_t cols, int l, float* edge,
-                                           int stride) {
-    if (EDGES) {
-        constexpr int kPer = (3 + LPR - 1) / LPR;
-        const int64_t head = row_head(row, cols);
-        const int64_t m = (cols - head) >> 2;
-        const int64_t tail0 = head + 4 * m;
-        const int nh = int(head), nt = int(cols - tail0);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const size_t span = size_t(cols) * 4;
-        for (int e = l; e < nh; e += LPR)
-            if (guard(row + e, 4, row, span)) cp_async4(edge + (e / LPR) * stride, row + e);
-        for (int e = l; e < nt; e += LPR)
-            if (guard(row + tail0 + e, 4, row, span)) cp_async4(edge + (kPer + e / LPR) * stride, row + tail0 + e);
-        bool pending = true;
-        auto add_edges = [&]() {
-            cp_async_wait_all();
-#pragma unroll
-            for (int k = 0; k < kPer; ++k)
-                if (l + k * LPR < nh) acc[0] += edge[k * stride];
-#pragma unroll
-            for (int k = 0; k < kPer; ++k)
-                if (l + k * LPR < nt) acc[1] += edge[(kPer + k) * stride];
-            pending = false;
-        };
-        const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
-        int64_t j = l;
-        for (; j + 3 * LPR < m; j += 4 * LPR) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = guard(rv + j + u * LPR, 16, row, span) ? ld_stream16(rv + j + u * LPR) : SumF32::neutral();
-            batch_fence(v);
-            if (pending) add_edges();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) acc[u] += SumF32::fold(v[u]);
-        }
-        if (pending) add_edges();
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (j + u * LPR < m && guard(rv + j + u * LPR, 16, row, span))
-                acc[u] += SumF32::fold(ld_stream16(rv + j + u * LPR));
-        }
-        return fold_array(acc);
-    }
+// Sum of lane l's share of one row, the row split among LPR lanes: the up to
+// 3 + 3 floats before the first and after the last whole vector, then the
+// row's 16-byte vectors l, l + LPR, ..., four in flight at a time.
+template <int LPR>
+__device__ __forceinline__ float row_share(const float* __restrict__ row, int64_t cols, int l) {
     const int64_t head = row_head(row, cols);
     const int64_t m = (cols - head) >> 2;
     const int64_t tail0 = head + 4 * m;
@@ -234,7 +187,7 @@ __device__ __forceinline__ float row_share(const float* __restrict__ row, int64_
 // Short rows.  Group g of warp w (lanes g*LPR .. g*LPR+LPR-1) sums row
 // (w + k * nwarps) * NG + g for k = 0, 1, ...; lane 0 of the group stores it.
 // The NG rows of one warp step are consecutive, so are their sums.
-template <int LPR, bool EDGES>
+template <int LPR>
 __global__ void __launch_bounds__(kGroupBlock)
 rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                     float* __restrict__ out) {
@@ -247,12 +200,10 @@ rowsum_group_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int
     const int64_t warp = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
     const int64_t nwarps = int64_t(gridDim.x) * (kGroupBlock / kWarpSize);
     const int64_t nsteps = (rows + NG - 1) / NG;
-    constexpr int kPer = (3 + LPR - 1) / LPR;
-    __shared__ float edge[EDGES ? 2 * kPer : 1][EDGES ? kGroupBlock : 1];  // the rows' edge floats
     for (int64_t k = warp; k < nsteps; k += nwarps) {
         const int64_t r = k * NG + grp;
         float s = 0.f;
-        if (r < rows) s = row_share<LPR, EDGES>(x + r * ld, cols, l, &edge[0][EDGES ? threadIdx.x : 0], kGroupBlock);
+        if (r < rows) s = row_share<LPR>(x + r * ld, cols, l);
         s = group_allreduce<LPR>(s);  // every lane takes part, in range or not
         if (l == 0 && r < rows && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = s;
     }
@@ -789,7 +740,7 @@ cudaError_t launch_fit(const float* x, int64_t rows, int64_t cols, int64_t ld, f
     return launch_pdl(rowsum_fit_kernel<LPR>, dim3(unsigned(blocks)), dim3(kGroupBlock), stream, x, rows, cols, ld, out);
 }
 
-template <int LPR, bool EDGES>
+template <int LPR>
 cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld, float* out, cudaStream_t stream) {
     constexpr int64_t kNG = kWarpSize / LPR;
     constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
@@ -797,8 +748,8 @@ cudaError_t launch_group(const float* x, int64_t rows, int64_t cols, int64_t ld,
     int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     // one step per warp, as in launch_fit
     if (blocks > 0x7fffffff) blocks = 0x7fffffff;
-    return launch_pdl(rowsum_group_kernel<LPR, EDGES>, dim3(unsigned(blocks)), dim3(kGroupBlock), stream, x, rows, cols,
-                      ld, out);
+    return launch_pdl(rowsum_group_kernel<LPR>, dim3(unsigned(blocks)), dim3(kGroupBlock), stream, x, rows, cols, ld,
+                      out);
 }
 
 }  // namespace
@@ -1038,14 +989,7 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
             default: return launch_fit<32>(x, rows, cols, ld, out, stream);
         }
     }
-    if (cols <= kGroupRowMaxCols) {
-        // rows that are not all 16-byte aligned and at least kGroupEdgeMinCols
-        // long take the variant that copies their edge floats
-        const bool edges =
-            cols >= kGroupEdgeMinCols && (reinterpret_cast<uintptr_t>(x) % 16 != 0 || ld % 4 != 0);
-        return edges ? launch_group<32, true>(x, rows, cols, ld, out, stream)
-                     : launch_group<32, false>(x, rows, cols, ld, out, stream);
-    }
+    if (cols <= kGroupRowMaxCols) return launch_group<32>(x, rows, cols, ld, out, stream);
     const int64_t blocks = rows < 0x7fffffff ? rows : 0x7fffffff;
     if (cols >= kCtaDeepCols)
         return launch_pdl(rowsum_cta_kernel<kCtaUnrollDeep, 4>, dim3(unsigned(blocks)), dim3(kCtaBlock), stream, x, rows,

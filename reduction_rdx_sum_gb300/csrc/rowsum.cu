@@ -543,15 +543,18 @@ rowsum_narrow_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     }
 }
 
-// Short rows that the short-row kernel would leave with half-empty load
-// slots (see rowsum_staged_lanes): tiles of whole rows staged as in the
-// narrow kernel, by one bulk copy each (24 KiB, 8 blocks per SM, so the
-// bytes in flight do not depend on the width), then summed from shared
-// memory by groups of LW lanes: lane l of a group adds words l, l + LW, ...
-// of its row in two alternating chains, the group's shuffle tree adds the
-// lanes, and its first lane stores the sum.  The lanes of a warp read
-// consecutive words of a row, so the reads meet no bank conflict whatever
-// the row's alignment.  The order depends on cols and LW only.
+// Staged rows (see rowsum_staged_lanes: short rows that the short-row kernel
+// would leave with half-empty load slots, and medium rows up to
+// kStagedMaxCols, contiguous or with gaps under kStagedMaxGap floats between
+// them): the span of a tile's rows, gaps included, is staged as in the
+// narrow kernel by one bulk copy (at most 24 KiB, 8 blocks per SM, so the
+// bytes in flight do not depend on the width), and row q is read at word
+// q * ld of it by a group of LW lanes: lane l adds words l, l + LW, ... of
+// the row in two alternating chains, the group's shuffle tree adds the
+// lanes, and its first lane stores the sum.  A group reads consecutive
+// words; the 32 / LW groups of a warp read rows ld words apart, which the
+// launcher keeps to at most 2 ways of bank sharing.  The order depends on
+// cols and LW only.
 template <int LW>
 __global__ void __launch_bounds__(kNarrowBlock)
 rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int64_t rows_per_tile,
@@ -586,10 +589,12 @@ rowsum_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, in
     }
 }
 
-// Short and medium rows with a leading dimension (ld > cols), where every
-// row has its own alignment: the rows of a tile are staged one bulk copy per
-// row, each row's 16-byte body into a slot of W words (a multiple of 4 with
-// 4 spare words in front), its up to 3 + 3 edge floats by plain loads, so
+// Rows with a leading dimension whose gap to the next row is kStagedMaxGap
+// floats or more (copying their span would read sectors without row data),
+// from kRowsStagedMinCols columns: the rows of a tile are staged one bulk
+// copy per row, each row's 16-byte body into a slot of W words (a multiple
+// of 4 with 4 spare words in front), its up to 3 + 3 edge floats by plain
+// loads, so
 // that row q's words occupy [q W + 4 - h, q W + 4 - h + cols) with h the
 // row's floats before its first 16-byte boundary.  W is padded so that the
 // kGroups rows a warp reads at once start LW words apart modulo 32: the
@@ -719,11 +724,12 @@ static int64_t rows_staged_slot(int64_t cols, int lw) {
     return w;
 }
 
-// Lanes per row of rowsum_rows_staged_kernel for rows with a leading
-// dimension (ld > cols), or 0 where the short-row, warp-per-row and
-// block-per-row kernels keep them: the same rule as for contiguous rows
-// (rows_staged has the same half-empty short-row slots to avoid), with
-// "aligned" meaning every row 16-byte aligned.
+// Lanes per row of rowsum_rows_staged_kernel, or 0 where other kernels take
+// the rows: rows with gaps of kStagedMaxGap floats or more between them, of
+// kRowsStagedMinCols to kStagedMaxCols columns (measured with gaps of 16
+// floats, 1 GiB spans: 1500-5000 columns 152-156 -> 147-150 us; below 1500
+// columns the per-row copies cost more than they save, 600 columns 154 ->
+// 170 us, 68 columns 197 -> 265).
 static int rowsum_rows_staged_lanes(const float*, int64_t cols, int64_t ld) {
     return ld - cols >= kStagedMaxGap && cols >= kRowsStagedMinCols && cols <= kStagedMaxCols ? 32 : 0;
 }

@@ -658,6 +658,71 @@ rowsum_rows_staged_kernel(const float* __restrict__ x, int64_t rows, int64_t col
     }
 }
 
+// Short rows whose power-of-two lane groups would run half empty and that the
+// staged kernels do not take (rows with wide gaps between them): groups of G
+// lanes (G = ceil(vecs / 4), not a power of two), 32 / G rows per warp step,
+// the lanes past the last whole group idle; otherwise as rowsum_fit_kernel
+// (at most four 16-byte vectors per lane in one load round, the edge floats
+// copied with cp.async ahead of the vector loads and added after them).  The
+// group's lanes are added by a shuffle-down tree in which lane l takes lane
+// l + off only while l + off < G, so lane 0 of each group ends with the sum
+// of its G lanes, in an order fixed by G.
+template <int G>
+__global__ void __launch_bounds__(kGroupBlock, 2048 / kGroupBlock)
+rowsum_fitg_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                   float* __restrict__ out) {
+    pdl_wait();     // the previous kernel in the stream has finished writing
+    pdl_release();  // the next one may be scheduled into SMs this grid frees
+    constexpr int NG = kWarpSize / G;
+    const int lane = threadIdx.x % kWarpSize;
+    const int grp = lane / G;
+    const int l = lane % G;
+    // one unit of NG rows per warp: the launcher sizes the grid to cover them
+    const int64_t k = (int64_t(blockIdx.x) * kGroupBlock + threadIdx.x) / kWarpSize;
+    __shared__ float edge[2][kGroupBlock];  // [head, tail][thread]
+    {
+        uint4 v[4];
+        int nh = 0, nt = 0;
+        float sc = 0.f;
+        const int64_t r = k * NG + grp;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (grp < NG && r < rows) {
+            const float* __restrict__ row = x + r * ld;
+            const int64_t head = row_head(row, cols);
+            const int64_t m = (cols - head) >> 2;
+            const int64_t tail0 = head + 4 * m;
+            const size_t span = size_t(cols) * 4;
+            nh = int(head);
+            nt = int(cols - tail0);
+            for (int e = l; e < nh; e += G)
+                if (guard(row + e, 4, row, span)) cp_async4(&edge[0][threadIdx.x], row + e);
+            for (int e = l; e < nt; e += G)
+                if (guard(row + tail0 + e, 4, row, span)) cp_async4(&edge[1][threadIdx.x], row + tail0 + e);
+            const uint4* __restrict__ rv = reinterpret_cast<const uint4*>(row + head);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (l + u * G < m && guard(rv + l + u * G, 16, row, span)) v[u] = ld_stream16(rv + l + u * G);
+            }
+        }
+        batch_fence(v);
+        cp_async_wait_all();
+        float acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = SumF32::fold(v[u]);
+        if (l < nh) sc += edge[0][threadIdx.x];  // the head float, then the tail float
+        if (l < nt) sc += edge[1][threadIdx.x];
+        acc[0] += sc;
+        float s = fold_array(acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_down_sync(kFullMask, s, off);
+            if (l + off < G) s += o;
+        }
+        if (l == 0 && grp < NG && r < rows && guard(out + r, 4, out, size_t(rows) * 4)) out[r] = s;
+    }
+}
+
 // Lanes per row: the fewest (a power of two, at most 32) that leave each lane
 // at most four 16-byte vectors of the row.
 int lanes_per_row(int64_t cols) {
@@ -732,6 +797,24 @@ static int64_t rows_staged_slot(int64_t cols, int lw) {
 // 170 us, 68 columns 197 -> 265).
 static int rowsum_rows_staged_lanes(const float*, int64_t cols, int64_t ld) {
     return ld - cols >= kStagedMaxGap && cols >= kRowsStagedMinCols && cols <= kStagedMaxCols ? 32 : 0;
+}
+
+// Lanes per row of rowsum_fitg_kernel, or 0 where the power-of-two groups
+// of rowsum_fit_kernel stay: rows that no staged kernel takes (see the
+// launcher) and whose power-of-two groups would fill their warp's load slots
+// at least a tenth less than groups of ceil(vecs / 4) lanes do (68-99 and
+// 132-163 columns, groups of 5, 6, 9 or 10 lanes: 68 columns 53 % against
+// 80 %, 160 columns 62 % against 94 %).
+static int rowsum_fitg_lanes(int64_t cols) {
+    if (cols < kNarrowMaxCols || cols > kFitRowMaxCols) return 0;
+    const int64_t vecs = cols / 4;
+    const int lpr = lanes_per_row(cols);
+    const int g = int((vecs + 3) / 4);
+    if (g != 5 && g != 6 && g != 9 && g != 10) return 0;  // the sizes the rule below can pick
+    // slots used per warp, over 128: vecs * (32 / lpr) for power-of-two
+    // groups, vecs * (32 / g) for groups of g; compare in integers
+    const int64_t pow2 = vecs * (kWarpSize / lpr), any = vecs * (kWarpSize / g);
+    return 10 * (any - pow2) >= 128 ? g : 0;
 }
 
 template <int LPR>
@@ -984,6 +1067,20 @@ cudaError_t rowsum_launch(const float* x, int64_t rows, int64_t cols, int64_t ld
         if (lw == 8) return launch_pdl(rowsum_staged_kernel<8>, grid, block, stream, x, rows, cols, ld, rpt, out);
         if (lw == 16) return launch_pdl(rowsum_staged_kernel<16>, grid, block, stream, x, rows, cols, ld, rpt, out);
         return launch_pdl(rowsum_staged_kernel<32>, grid, block, stream, x, rows, cols, ld, rpt, out);
+    }
+    if (const int g = rowsum_fitg_lanes(cols)) {
+        const int64_t ng = kWarpSize / g;
+        const int64_t nsteps = (rows + ng - 1) / ng;
+        constexpr int64_t kWarpsPerBlock = kGroupBlock / kWarpSize;
+        const int64_t blocks = (nsteps + kWarpsPerBlock - 1) / kWarpsPerBlock;  // one unit per warp
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;  // would take more than 5 * 10^10 rows
+        const dim3 grid{unsigned(blocks)}, block{unsigned(kGroupBlock)};
+        switch (g) {
+            case 5: return launch_pdl(rowsum_fitg_kernel<5>, grid, block, stream, x, rows, cols, ld, out);
+            case 6: return launch_pdl(rowsum_fitg_kernel<6>, grid, block, stream, x, rows, cols, ld, out);
+            case 9: return launch_pdl(rowsum_fitg_kernel<9>, grid, block, stream, x, rows, cols, ld, out);
+            default: return launch_pdl(rowsum_fitg_kernel<10>, grid, block, stream, x, rows, cols, ld, out);
+        }
     }
     if (cols <= kFitRowMaxCols) {
         switch (lanes_per_row(cols)) {

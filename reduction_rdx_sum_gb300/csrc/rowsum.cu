@@ -11,7 +11,9 @@
 //   * short rows (cols <= kFitRowMaxCols): a group of LPR lanes per row, each
 //     lane holding at most four 16-byte vectors of the row, so a warp sums
 //     32/LPR consecutive rows per step; the loads of kRowSteps steps are
-//     issued together before any of them is reduced;
+//     issued together before any of them is reduced; where a power of two
+//     of lanes would leave the slots half empty, groups of 5, 6, 9 or 10
+//     lanes (see rowsum_fitg_lanes);
 //   * staged rows (see rowsum_staged_lanes): short rows that would leave
 //     those lanes' load slots half empty, and medium rows up to
 //     kStagedMaxCols, are staged like narrow rows, 24 KiB of whole rows per

@@ -6,6 +6,7 @@ For quick timings and for profilers (one kernel, a few launches, a chosen size):
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 262144 --cols 256
     python -m reduction_rdx_sum_gb300.runop --config c5_sum_bf16     # a workload of the suite
     python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 16777216 --cols 16 --offset 1
+    python -m reduction_rdx_sum_gb300.runop --op rowsum_f32 --rows 2000000 --cols 132 --ld 148   # rows 148 floats apart
     python -m reduction_rdx_sum_gb300.runop --op ladder_partials --version 2 --n 262144 --input page
 
 Before each timed call the L2 is flushed (a write of 512 MiB, then a read of
@@ -78,6 +79,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--offset", type=int, default=0,
                     help="start the input this many elements into its allocation (a base off 16-byte alignment)")
+    ap.add_argument("--ld", type=int, default=None,
+                    help="rowsum_f32: rows start every LD floats (a leading dimension >= cols; default cols)")
     ap.add_argument("--version", type=int, default=5, choices=range(1, 6),
                     help="the page's block-reduction version for ladder_partials / ladder_sum")
     ap.add_argument("--input", choices=("seeded", "page"), default="seeded",
@@ -85,6 +88,8 @@ def main(argv=None) -> int:
     args = ap.parse_args(argv)
     if args.offset < 0:
         ap.error("--offset must be >= 0")
+    if args.ld is not None and (args.op != "rowsum_f32" or args.ld < args.cols):
+        ap.error("--ld applies to --op rowsum_f32 and must be >= --cols")
     if (args.op is None) == (args.config is None):
         ap.error("give exactly one of --op and --config")
 
@@ -106,10 +111,16 @@ def main(argv=None) -> int:
         x = torch.from_numpy((np.arange(args.n) % 7).astype(np.float32)).to(dev)
     else:
         x = make_input(args.op, args.n, args.rows, args.cols, args.seed, dev)
-    if args.offset:
+    strided = args.ld is not None and args.ld > args.cols
+    if strided:  # the same rows, ld floats apart (the gaps zero)
+        buf = torch.zeros(args.rows * args.ld + args.offset, dtype=x.dtype, device=dev)
+        wide = buf[args.offset:].view(args.rows, args.ld)
+        wide[:, :args.cols].copy_(x)
+        x = wide[:, :args.cols]
+    elif args.offset:
         buf = torch.empty(x.numel() + args.offset, dtype=x.dtype, device=dev)
         x = buf[args.offset:].view(x.shape).copy_(x)
-    fn = entry(args.op, args.version)
+    fn = abi.rdx_rowsum_strided_f32 if strided else entry(args.op, args.version)
     stream = torch.cuda.current_stream(dev)
     flush = None if args.no_flush else L2Flush(dev)
     nbytes = x.numel() * x.element_size()

@@ -22,3 +22,10 @@ def test_every_workload_has_an_entry_point():
 def test_negative_offset_rejected():
     with pytest.raises(SystemExit):
         runop.main(["--op", "rowsum_f32", "--offset", "-1"])
+
+
+def test_leading_dimension_only_for_row_sums_and_not_below_cols():
+    with pytest.raises(SystemExit):
+        runop.main(["--op", "sum_f32", "--ld", "10"])
+    with pytest.raises(SystemExit):
+        runop.main(["--op", "rowsum_f32", "--rows", "4", "--cols", "8", "--ld", "7"])
